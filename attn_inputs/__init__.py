@@ -1,0 +1,196 @@
+"""Seeded synthetic inputs for the exact attention forward.
+
+Q, K and V are i.i.d. N(0, 1), as in the benchmark shapes of "Lecture 6 --
+FlashAttention-2" (Benchmark task) and the attention-layer notebook
+("FlashAttention-2 in an attention layer", Numerical equivalence), where the
+inputs are plain Gaussian tensors.
+
+Generator, named so that seeds reproduce on any machine and torch version:
+
+* SplitMix64 (Steele, Lea & Flood, "Fast splittable pseudorandom number
+  generators", OOPSLA 2014), used as a counter-based stream: output ``o`` of
+  seed ``s`` is ``mix(s + (o + 1) * 0x9E3779B97F4A7C15 mod 2**64)``, which is
+  the sequential generator started from state ``s``.
+* A uniform double in [0, 1) from the top 53 bits of each output.
+* Box-Muller (Box & Muller, 1958): outputs ``2p`` and ``2p + 1`` give the
+  normal pair ``p``; ``r = sqrt(-2 ln(1 - u0))``, even index ``r cos(2 pi u1)``,
+  odd index ``r sin(2 pi u1)``.
+* Each normal is rounded to fp32, then to the 16-bit dtype, both
+  round-to-nearest-even.  Q, K and V draw consecutive normals (Q first).
+
+This module holds none of the attention arithmetic.  The oracle and the CUDA
+path both take their inputs from here and from nowhere else.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+GAMMA = 0x9E3779B97F4A7C15
+_M1 = 0xBF58476D1CE4E5B9
+_M2 = 0x94D049BB133111EB
+_CHUNK = 1 << 22
+
+DTYPES = ("fp16", "bf16")
+DTYPE_CODE = {"fp16": 0, "bf16": 1}
+
+
+def splitmix64(seed: int, start: int, count: int) -> np.ndarray:
+    """Outputs ``start .. start+count-1`` of SplitMix64 seeded with ``seed``."""
+    idx = np.arange(start + 1, start + count + 1, dtype=np.uint64)
+    z = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + idx * np.uint64(GAMMA)
+    z = (z ^ (z >> np.uint64(30))) * np.uint64(_M1)
+    z = (z ^ (z >> np.uint64(27))) * np.uint64(_M2)
+    return z ^ (z >> np.uint64(31))
+
+
+def uniform53(words: np.ndarray) -> np.ndarray:
+    """Map 64-bit words to doubles in [0, 1) using their top 53 bits."""
+    return (words >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def normals(seed: int, start: int, count: int) -> np.ndarray:
+    """Standard normals ``start .. start+count-1`` of the stream (float64)."""
+    if count <= 0:
+        return np.zeros(0, dtype=np.float64)
+    p0 = start // 2
+    p1 = (start + count - 1) // 2 + 1
+    w = splitmix64(seed, 2 * p0, 2 * (p1 - p0)).reshape(-1, 2)
+    u0 = uniform53(w[:, 0])
+    u1 = uniform53(w[:, 1])
+    r = np.sqrt(-2.0 * np.log1p(-u0))
+    theta = (2.0 * math.pi) * u1
+    z = np.empty((p1 - p0, 2), dtype=np.float64)
+    z[:, 0] = r * np.cos(theta)
+    z[:, 1] = r * np.sin(theta)
+    z = z.reshape(-1)
+    off = start - 2 * p0
+    return z[off:off + count]
+
+
+def round_fp32_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round finite fp32 values to bf16 (nearest-even); returned as fp32."""
+    bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (bits >> np.uint32(16)) & np.uint32(1)
+    r = (bits + np.uint32(0x7FFF) + lsb) & np.uint32(0xFFFF0000)
+    return r.view(np.float32)
+
+
+def round_to_dtype(x64: np.ndarray, dtype: str) -> np.ndarray:
+    """fp64 -> fp32 -> ``dtype`` (both nearest-even); returned as fp32."""
+    x32 = x64.astype(np.float32)
+    if dtype == "fp16":
+        return x32.astype(np.float16).astype(np.float32)
+    if dtype == "bf16":
+        return round_fp32_to_bf16(x32)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+def gaussian_tensor(seed: int, start: int, shape, dtype: str) -> np.ndarray:
+    """A tensor of ``prod(shape)`` consecutive normals, rounded to ``dtype``.
+
+    The result is float32 holding values exactly representable in ``dtype``.
+    """
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float32)
+    for c0 in range(0, n, _CHUNK):
+        c1 = min(n, c0 + _CHUNK)
+        out[c0:c1] = round_to_dtype(normals(seed, start + c0, c1 - c0), dtype)
+    return out.reshape(shape)
+
+
+@dataclasses.dataclass
+class QKV:
+    """One input set: ``q, k, v`` are float32 ``[B, H, S, D]`` arrays whose
+    values are exactly representable in ``dtype``."""
+
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    dtype: str
+    seed: int
+    qk_mult: float
+
+    @property
+    def shape(self):
+        return self.q.shape
+
+
+def make_qkv(B: int, H: int, S: int, D: int, dtype: str, seed: int,
+             qk_mult: float = 1.0) -> QKV:
+    """Q, K, V i.i.d. N(0,1) from ``seed`` (Q, then K, then V in the stream).
+
+    ``qk_mult`` multiplies Q and K after rounding; it must be a power of two so
+    the product is exact in the 16-bit dtype (the stress set uses 4).
+    """
+    if dtype not in DTYPES:
+        raise ValueError(f"unknown dtype {dtype!r}")
+    m, e = math.frexp(qk_mult)
+    if qk_mult <= 0 or m != 0.5:
+        raise ValueError("qk_mult must be a positive power of two")
+    n = B * H * S * D
+    shape = (B, H, S, D)
+    q = gaussian_tensor(seed, 0, shape, dtype)
+    k = gaussian_tensor(seed, n, shape, dtype)
+    v = gaussian_tensor(seed, 2 * n, shape, dtype)
+    if qk_mult != 1.0:
+        q *= np.float32(qk_mult)
+        k *= np.float32(qk_mult)
+    return QKV(q=q, k=k, v=v, dtype=dtype, seed=seed, qk_mult=qk_mult)
+
+
+# --------------------------------------------------------------------------
+# The workloads: sizes, dtypes, masks and seeds of the benchmark shapes.
+# --------------------------------------------------------------------------
+
+SWEEP_S = (512, 1024, 2048, 4096, 8192, 16384, 4097)
+SWEEP_D = (64, 128)
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    S: int
+    D: int
+    dtype: str
+    causal: tuple  # the mask modes run on this input set
+    seed: int
+    qk_mult: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    def inputs(self) -> QKV:
+        return make_qkv(self.B, self.H, self.S, self.D, self.dtype, self.seed,
+                        self.qk_mult)
+
+
+def sweep_workloads():
+    """B=2, H=16 sweep; seed = 4 + index over (S, D, dtype) in that nesting."""
+    out = []
+    idx = 0
+    for S in SWEEP_S:
+        for D in SWEEP_D:
+            for dt in DTYPES:
+                out.append(Workload(f"sweep_S{S}_D{D}_{dt}", 2, 16, S, D, dt,
+                                    (False, True), 4 + idx))
+                idx += 1
+    return out
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, 2, 128, 64, "fp16", (False,), 0),
+    "s2048_d64": Workload("B2_H16_S2048_D64_fp16_causal", 2, 16, 2048, 64,
+                        "fp16", (True,), 1),
+    "s2048_d128": Workload("B1_H32_S2048_D128_fp16_causal", 1, 32, 2048, 128,
+                         "fp16", (True,), 2),
+    "s8192_d128": Workload("B2_H16_S8192_D128_bf16", 2, 16, 8192, 128, "bf16",
+                          (False, True), 3),
+    "s8192_d128_x4": Workload("B2_H16_S8192_D128_bf16_QKx4", 2, 16, 8192, 128,
+                             "bf16", (False, True), 3, 4.0),
+}

@@ -1,0 +1,66 @@
+"""The seeded input generator: published SplitMix64 outputs, Box-Muller
+statistics, exact rounding to the 16-bit dtypes and the workload seeds."""
+import numpy as np
+import pytest
+import torch
+
+import attn_inputs as ai
+
+
+def test_splitmix64_published_vectors():
+    # Reference outputs of SplitMix64 started from state 1234567 (the test
+    # vector of the published C implementation by S. Vigna).
+    want = [6457827717110365317, 3203168211198807973, 9817491932198370423,
+            4593380528125082431, 16408922859458223821]
+    assert [int(x) for x in ai.splitmix64(1234567, 0, 5)] == want
+
+
+def test_stream_is_counter_based():
+    a = ai.splitmix64(99, 0, 1000)
+    b = ai.splitmix64(99, 600, 400)
+    np.testing.assert_array_equal(a[600:], b)
+    z = ai.normals(7, 0, 1001)
+    np.testing.assert_array_equal(z[333:1001], ai.normals(7, 333, 668))
+
+
+def test_normal_statistics():
+    z = ai.normals(5, 0, 1 << 20)
+    assert abs(z.mean()) < 5e-3
+    assert abs(z.std() - 1.0) < 5e-3
+    # fourth moment of N(0,1) is 3
+    assert abs((z ** 4).mean() - 3.0) < 0.05
+
+
+@pytest.mark.parametrize("dtype,tdt", [("fp16", torch.float16),
+                                       ("bf16", torch.bfloat16)])
+def test_rounding_matches_torch_rne(dtype, tdt):
+    x = ai.normals(11, 0, 100000) * 3.0
+    ours = ai.round_to_dtype(x, dtype)
+    ref = torch.from_numpy(x.astype(np.float32)).to(tdt).to(torch.float32)
+    np.testing.assert_array_equal(ours, ref.numpy())
+
+
+def test_make_qkv_shapes_and_exactness():
+    w = ai.make_qkv(1, 2, 33, 8, "bf16", 4)
+    assert w.q.shape == (1, 2, 33, 8) and w.q.dtype == np.float32
+    for t in (w.q, w.k, w.v):
+        back = torch.from_numpy(t).to(torch.bfloat16).to(torch.float32).numpy()
+        np.testing.assert_array_equal(back, t)
+    n = 2 * 33 * 8
+    np.testing.assert_array_equal(
+        w.k.reshape(-1), ai.round_to_dtype(ai.normals(4, n, n), "bf16"))
+    x4 = ai.make_qkv(1, 2, 33, 8, "bf16", 4, qk_mult=4.0)
+    np.testing.assert_array_equal(x4.q, 4 * w.q)
+    np.testing.assert_array_equal(x4.v, w.v)
+    with pytest.raises(ValueError):
+        ai.make_qkv(1, 1, 4, 4, "bf16", 0, qk_mult=3.0)
+
+
+def test_sweep_seeds():
+    ws = ai.sweep_workloads()
+    assert len(ws) == 28
+    assert [w.seed for w in ws] == list(range(4, 32))
+    assert (ws[0].S, ws[0].D, ws[0].dtype) == (512, 64, "fp16")
+    assert (ws[3].S, ws[3].D, ws[3].dtype) == (512, 128, "bf16")
+    assert (ws[-1].S, ws[-1].D, ws[-1].dtype) == (4097, 128, "bf16")
+    assert all(w.B == 2 and w.H == 16 for w in ws)
