@@ -1,0 +1,144 @@
+"""Exact softmax-attention forward on GB300 (sm_103a).
+
+A thin ctypes binding over ``libfattn.so`` (C ABI in ``include/fattn.h``):
+argument marshalling only.  Every step of the computation runs in the CUDA
+kernels of that library; there is no other implementation to fall back to, and
+calling into a missing library raises.
+
+    o, lse = forward(q, k, v, causal=True)      # torch tensors on a GB300
+
+``q, k, v``: contiguous ``[B, H, S, D]`` fp16 or bf16 CUDA tensors, D in
+{64, 128}.  Returns ``o`` (same shape and dtype) and ``lse`` (``[B, H, S]``
+fp32, natural log of the row's softmax normaliser over scaled scores).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfattn.so")
+
+FATTN_OK = 0
+FATTN_ERR_INVALID_ARG = -1
+FATTN_ERR_UNSUPPORTED = -2
+FATTN_ERR_MISALIGNED = -3
+FATTN_ERR_TOO_LARGE = -4
+FATTN_ERR_LAUNCH = -5
+FATTN_ERR_PIPELINE_TIMEOUT = -6
+FATTN_ERR_CUDA = -7
+FATTN_FP16 = 0
+FATTN_BF16 = 1
+
+_lib = None
+
+
+class FattnError(RuntimeError):
+    """A non-zero status from the library."""
+
+    def __init__(self, status: int, what: str = "fattn_fwd"):
+        self.status = status
+        super().__init__(f"{what} failed: {status} ({fattn_error_string(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises ImportError if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        l = ctypes.CDLL(LIB_PATH)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        ip = ctypes.POINTER(ctypes.c_int)
+        l.fattn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+        l.fattn_fwd.restype = i
+        l.fattn_last_error.argtypes = [vp, ip]
+        l.fattn_last_error.restype = i
+        l.fattn_error_string.argtypes = [i]
+        l.fattn_error_string.restype = ctypes.c_char_p
+        l.fattn_plan.argtypes = [i, i, i, i, i, ip, ip, ip, ip, ip, ip]
+        l.fattn_plan.restype = i
+        l.fattn_version.argtypes = []
+        l.fattn_version.restype = i
+        _lib = l
+    return _lib
+
+
+# ------------------------------------------------------- the C ABI, by name
+
+def fattn_fwd(q, k, v, o, lse, B, H, S, D, causal, scale, dtype, stream) -> int:
+    """``fattn_fwd`` with integer device pointers and an integer stream."""
+    return lib().fattn_fwd(q, k, v, o, lse, B, H, S, D, int(causal),
+                           float(scale), dtype, stream)
+
+
+def fattn_last_error(stream=0):
+    """(status, (where, block)) of the last kernel error on this device."""
+    detail = (ctypes.c_int * 2)()
+    rc = lib().fattn_last_error(stream, detail)
+    return rc, (detail[0], detail[1])
+
+
+def fattn_error_string(status: int) -> str:
+    return lib().fattn_error_string(status).decode()
+
+
+def fattn_plan(B, H, S, D, causal=False) -> dict:
+    """The launch ``fattn_fwd`` would make (grid, block, smem, units...)."""
+    vals = [ctypes.c_int() for _ in range(6)]
+    rc = lib().fattn_plan(B, H, S, D, int(causal), *[ctypes.byref(x) for x in vals])
+    if rc != FATTN_OK:
+        raise FattnError(rc, "fattn_plan")
+    keys = ("grid", "block", "smem_bytes", "units", "q_tiles_per_unit",
+            "kv_stages")
+    return {k_: x.value for k_, x in zip(keys, vals)}
+
+
+def fattn_version() -> int:
+    return lib().fattn_version()
+
+
+# ------------------------------------------------------------ torch wrapper
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.float16:
+        return FATTN_FP16
+    if t.dtype == torch.bfloat16:
+        return FATTN_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; expected float16 or bfloat16")
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None,
+            out=None, lse=None, stream=None):
+    """Attention forward on the current CUDA stream (or ``stream``).
+
+    Allocates ``o`` and ``lse`` with torch on q's device unless given.
+    Raises FattnError on any non-zero status."""
+    import torch
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share one [B, H, S, D] shape")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share a dtype")
+    if not q.is_cuda:
+        raise ValueError("q, k, v must be CUDA tensors")
+    B, H, S, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                   lse.data_ptr(), B, H, S, D, causal, scale, _dtype_code(q),
+                   stream.cuda_stream)
+    if rc != FATTN_OK:
+        raise FattnError(rc)
+    return out, lse

@@ -1,0 +1,323 @@
+// Host side of the C ABI declared in include/fattn.h: argument validation,
+// tensor-map encoding, launch planning, the device status block.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "fattn.h"
+#include "fattn_launch.cuh"
+#include "fattn_status.h"
+
+namespace fattn {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultTimeoutNs = 1000000000ull;  // 1 s per wait
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
+                                   void*, const cuuint64_t*, const cuuint64_t*,
+                                   const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+using AddressRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+
+struct DriverFns {
+  EncodeTiledFn encode = nullptr;
+  AddressRangeFn range = nullptr;
+};
+
+// Driver entry points through the runtime, so the library loads (and its
+// host-side checks run) on machines without a driver.
+const DriverFns& driver() {
+  static const DriverFns fns = [] {
+    DriverFns f;
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.encode = reinterpret_cast<EncodeTiledFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.range = reinterpret_cast<AddressRangeFn>(p);
+    cudaGetLastError();
+    return f;
+  }();
+  return fns;
+}
+
+struct DeviceState {
+  bool init = false;
+  bool supported = false;
+  int sms = 0;
+  int* status = nullptr;  // kStatusWords ints, device memory
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+unsigned long long wait_timeout_ns() {
+  static const unsigned long long t = [] {
+    const char* s = std::getenv("FATTN_WAIT_TIMEOUT_MS");
+    if (s && *s) {
+      const long long ms = std::atoll(s);
+      if (ms > 0 && ms < 600000) return (unsigned long long)ms * 1000000ull;
+    }
+    return kDefaultTimeoutNs;
+  }();
+  return t;
+}
+
+// The current device's state, created on first use (device query, status
+// block allocation).  Must not first run inside a stream capture.
+int current_device(DeviceState** out, int* dev_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return kErrUnsupported;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return kErrUnsupported;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.init) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return kErrCuda;
+    }
+    d.sms = sms;
+    d.supported = (major == 10 && minor == 3);
+    if (d.supported) {
+      if (cudaMalloc(&d.status, sizeof(int) * kStatusWords) != cudaSuccess ||
+          cudaMemset(d.status, 0, sizeof(int) * kStatusWords) != cudaSuccess) {
+        cudaGetLastError();
+        if (d.status) cudaFree(d.status);
+        d.status = nullptr;
+        return kErrCuda;
+      }
+    }
+    d.init = true;
+  }
+  if (!d.supported) return kErrUnsupported;
+  *out = &d;
+  if (dev_out) *dev_out = dev;
+  return kOk;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a);
+  const uintptr_t y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// The buffer must be device (or managed) memory of the current device, and
+// its allocation must hold ``bytes`` from ``p``.
+int check_device_buffer(const void* p, size_t bytes, int dev) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return kErrInvalidArg;
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return kErrInvalidArg;
+  if (attr.type == cudaMemoryTypeDevice && attr.device != dev) return kErrInvalidArg;
+  const DriverFns& f = driver();
+  if (!f.range) return kErrCuda;
+  CUdeviceptr base = 0;
+  size_t size = 0;
+  if (f.range(&base, &size, reinterpret_cast<CUdeviceptr>(p)) != CUDA_SUCCESS)
+    return kErrInvalidArg;
+  if (reinterpret_cast<uintptr_t>(p) + bytes > (uintptr_t)base + size)
+    return kErrInvalidArg;
+  return kOk;
+}
+
+int encode_bhsd(CUtensorMap* tm, const void* ptr, int S, int BH, int D,
+                bool bf16) {
+  const DriverFns& f = driver();
+  if (!f.encode) return kErrCuda;
+  // [BH, S, D] viewed as 3-D (D innermost); one box is 64 columns (128 bytes,
+  // the swizzle span) x 128 rows of one head.  Rows past S read as zeros.
+  cuuint64_t gdim[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
+  cuuint64_t gstride[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * (cuuint64_t)D * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kSwizzleChunkCols, (cuuint32_t)kBM, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = f.encode(
+      tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+      3, const_cast<void*>(ptr), gdim, gstride, box, estride,
+      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? kOk : kErrCuda;
+}
+
+struct Plan {
+  int qt, ns, threads, smem, units_per_head, total_units;
+};
+
+int host_checks(int B, int H, int S, int D, Plan* plan) {
+  if (B < 1 || H < 1 || S < 1) return kErrInvalidArg;
+  if (D != 64 && D != 128) return kErrUnsupported;
+  const long long rows = (long long)B * H * S;
+  if (rows > INT_MAX) return kErrTooLarge;
+  if (D == 64) {
+    plan->qt = FwdConfig<64>::QT;
+    plan->ns = FwdConfig<64>::NS;
+    plan->threads = FwdShape<64>::kThreads;
+    plan->smem = FwdShape<64>::kSmem;
+  } else {
+    plan->qt = FwdConfig<128>::QT;
+    plan->ns = FwdConfig<128>::NS;
+    plan->threads = FwdShape<128>::kThreads;
+    plan->smem = FwdShape<128>::kSmem;
+  }
+  const int rows_per_unit = kBM * plan->qt;
+  plan->units_per_head = (S + rows_per_unit - 1) / rows_per_unit;
+  const long long total = (long long)B * H * plan->units_per_head;
+  if (total > INT_MAX) return kErrTooLarge;
+  plan->total_units = (int)total;
+  return kOk;
+}
+
+}  // namespace
+}  // namespace fattn
+
+using namespace fattn;
+
+extern "C" {
+
+FATTN_API int fattn_version(void) { return 100; }
+
+FATTN_API const char* fattn_error_string(int status) {
+  switch (status) {
+    case FATTN_OK: return "ok";
+    case FATTN_ERR_INVALID_ARG: return "invalid argument";
+    case FATTN_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case FATTN_ERR_MISALIGNED: return "misaligned pointer";
+    case FATTN_ERR_TOO_LARGE: return "problem too large";
+    case FATTN_ERR_LAUNCH: return "kernel launch failed";
+    case FATTN_ERR_PIPELINE_TIMEOUT: return "device pipeline wait timed out";
+    case FATTN_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+FATTN_API int fattn_plan(int B, int H, int S, int D, int causal, int* grid,
+                         int* block, int* smem_bytes, int* units,
+                         int* q_tiles_per_unit, int* kv_stages) {
+  (void)causal;
+  Plan plan;
+  const int rc = host_checks(B, H, S, D, &plan);
+  if (rc != kOk) return rc;
+  int g = plan.total_units;
+  DeviceState* ds = nullptr;
+  if (current_device(&ds, nullptr) == kOk && ds->sms < g) g = ds->sms;
+  if (grid) *grid = g;
+  if (block) *block = plan.threads;
+  if (smem_bytes) *smem_bytes = plan.smem;
+  if (units) *units = plan.total_units;
+  if (q_tiles_per_unit) *q_tiles_per_unit = plan.qt;
+  if (kv_stages) *kv_stages = plan.ns;
+  return kOk;
+}
+
+FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o,
+                        float* lse, int B, int H, int S, int D, int causal,
+                        float scale, int dtype, fattn_stream_t stream) {
+  // ---- host-side checks, nothing enqueued yet
+  if (!q || !k || !v || !o || !lse) return FATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  Plan plan;
+  int rc = host_checks(B, H, S, D, &plan);
+  if (rc != kOk) return rc;
+  if (dtype != FATTN_FP16 && dtype != FATTN_BF16) return FATTN_ERR_UNSUPPORTED;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  if ((a16 & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return FATTN_ERR_MISALIGNED;
+  const size_t rows = (size_t)B * H * S;
+  const size_t tbytes = rows * (size_t)D * 2;
+  const size_t lbytes = rows * sizeof(float);
+  if (overlaps(o, tbytes, q, tbytes) || overlaps(o, tbytes, k, tbytes) ||
+      overlaps(o, tbytes, v, tbytes) || overlaps(lse, lbytes, q, tbytes) ||
+      overlaps(lse, lbytes, k, tbytes) || overlaps(lse, lbytes, v, tbytes) ||
+      overlaps(lse, lbytes, o, tbytes))
+    return FATTN_ERR_INVALID_ARG;
+
+  // ---- device checks
+  DeviceState* ds = nullptr;
+  int dev = 0;
+  rc = current_device(&ds, &dev);
+  if (rc != kOk) return rc;
+  if ((rc = check_device_buffer(q, tbytes, dev)) != kOk) return rc;
+  if ((rc = check_device_buffer(k, tbytes, dev)) != kOk) return rc;
+  if ((rc = check_device_buffer(v, tbytes, dev)) != kOk) return rc;
+  if ((rc = check_device_buffer(o, tbytes, dev)) != kOk) return rc;
+  if ((rc = check_device_buffer(lse, lbytes, dev)) != kOk) return rc;
+
+  const bool bf16 = dtype == FATTN_BF16;
+  const int BH = B * H;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (encode_bhsd(&tm_q, q, S, BH, D, bf16) != kOk ||
+      encode_bhsd(&tm_k, k, S, BH, D, bf16) != kOk ||
+      encode_bhsd(&tm_v, v, S, BH, D, bf16) != kOk)
+    return FATTN_ERR_CUDA;
+
+  LaunchArgs a;
+  a.tm_q = &tm_q;
+  a.tm_k = &tm_k;
+  a.tm_v = &tm_v;
+  a.params.o = o;
+  a.params.lse = lse;
+  a.params.status = ds->status;
+  a.params.S = S;
+  a.params.BH = BH;
+  a.params.n_kv_tiles = (S + kBN - 1) / kBN;
+  a.params.n_units = plan.units_per_head;
+  a.params.total_units = plan.total_units;
+  a.params.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  a.params.timeout_ns = wait_timeout_ns();
+  a.grid = plan.total_units < ds->sms ? plan.total_units : ds->sms;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+
+  const cudaError_t e = D == 64 ? launch_fwd_d64(causal != 0, bf16, a)
+                                : launch_fwd_d128(causal != 0, bf16, a);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FATTN_ERR_LAUNCH;
+  }
+  return FATTN_OK;
+}
+
+FATTN_API int fattn_last_error(fattn_stream_t stream, int* detail) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return FATTN_ERR_CUDA;
+  }
+  DeviceState* ds = nullptr;
+  const int rc = current_device(&ds, nullptr);
+  if (rc != kOk) return rc;
+  int h[kStatusWords] = {0, 0, 0, 0};
+  if (cudaMemcpy(h, ds->status, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(ds->status, 0, sizeof(h)) != cudaSuccess) {
+    cudaGetLastError();
+    return FATTN_ERR_CUDA;
+  }
+  if (detail) {
+    detail[0] = h[1];
+    detail[1] = h[2];
+  }
+  return h[0];
+}
+
+}  // extern "C"

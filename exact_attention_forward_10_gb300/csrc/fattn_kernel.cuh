@@ -1,0 +1,580 @@
+// Exact softmax-attention forward for sm_103a (GB300): O and the per-row LSE.
+//
+// What it computes (the plain definition, reached tile by tile):
+//   O = softmax(scale * Q K^T [+ causal mask]) V,  LSE = m + ln(sum exp(s - m))
+// with the online-softmax recurrence of "FlashAttention V2", section 3 (the
+// unnormalised accumulator is rescaled by exp(m_old - m_new) per key tile and
+// divided by the row sum once at the end) and the loop order of section 2
+// (query tile outer, key/value tiles inner, O written once).  Causal masking
+// keeps key <= query and stops at the diagonal tile; keys past S are removed
+// ("FlashAttention-2 in an attention layer", Triton FA2 kernel).
+//
+// GB300 structure (one persistent CTA per SM):
+//   * QT query tiles of 128 rows per work unit share every K/V tile.
+//   * load warp:   TMA (128-byte swizzle) Q once per unit; K_j, V_j through an
+//                  NS-stage mbarrier ring.
+//   * MMA warp:    one thread issues tcgen05.mma: S_i = Q_i K_j^T into TMEM
+//                  (fp32, 128 lanes x 128 columns), then O_i += P_i V_j with
+//                  P_i read from TMEM (16-bit, aliasing S_i) and O_i kept in
+//                  TMEM for the whole unit.
+//   * softmax warpgroup per query tile: thread r owns row r (TMEM lane r):
+//                  tcgen05.ld of its score row, mask, row max, exp2 with the
+//                  scale folded into one FFMA, row sum, 16-bit P back to TMEM.
+//                  (m, l) live in registers; no shuffles are needed because a
+//                  row never leaves its thread.
+//   * correction warpgroup: rescales O_i in TMEM only when some row's max
+//                  moved (alpha != 1), and runs the epilogue: one 1/l per row,
+//                  cast to 16-bit, vector stores of O and the LSE.
+// Every wait is bounded; a timeout records an error in the device status
+// block and the CTA unwinds (frees TMEM, waits for its own copies) instead of
+// hanging.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "fattn_status.h"
+#include "ptx.cuh"
+
+namespace fattn {
+
+constexpr int kBM = 128;  // query rows per tile (one TMEM lane each)
+constexpr int kBN = 128;  // keys per K/V tile
+constexpr int kSwizzleChunkCols = 64;           // 128 bytes of 16-bit values
+constexpr int kChunkBytes = kBM * 128;          // one [128 rows, 64 cols] chunk
+constexpr uint32_t kTmemCols = 512;
+
+struct FwdParams {
+  void* o;            // [BH, S, D] 16-bit
+  float* lse;         // [BH, S] fp32
+  int* status;        // device status block (kStatusWords ints)
+  int S;
+  int BH;
+  int n_kv_tiles;     // ceil(S / kBN)
+  int n_units;        // work units per head: ceil(S / (kBM * QT))
+  int total_units;    // BH * n_units
+  float scale_log2;   // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+template <int D, int QT, int NS>
+struct FwdLayout {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kTileBytes = kBM * D * 2;
+  static constexpr int kQ = 0;
+  static constexpr int kKV = kQ + QT * kTileBytes;
+  static constexpr int kBars = kKV + NS * kTileBytes;
+  // barrier slots (8 bytes each)
+  static constexpr int bQFull = 0;
+  static constexpr int bQEmpty = bQFull + QT;
+  static constexpr int bKVFull = bQEmpty + QT;
+  static constexpr int bKVEmpty = bKVFull + NS;
+  static constexpr int bSFull = bKVEmpty + NS;
+  static constexpr int bPFull = bSFull + QT;
+  static constexpr int bStats = bPFull + QT;
+  static constexpr int bOReady = bStats + QT;
+  static constexpr int bPVDone = bOReady + QT;
+  static constexpr int bOEmpty = bPVDone + QT;
+  static constexpr int bDrain = bOEmpty + QT;
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int kMisc = kBars + kNumBars * 8;   // tmem base, abort flag
+  static constexpr int kAlpha = kMisc + 16;            // float [QT][128]
+  static constexpr int kRowL = kAlpha + QT * kBM * 4;  // float [QT][128]
+  static constexpr int kRowM = kRowL + QT * kBM * 4;   // float [QT][128]
+  static constexpr int kEnd = kRowM + QT * kBM * 4;
+  static constexpr int kSmemBytes = kEnd + 1024;       // + alignment slack
+  // TMEM columns
+  __host__ __device__ static constexpr uint32_t colS(int i) { return 128u * i; }
+  __host__ __device__ static constexpr uint32_t colO(int i) { return 128u * QT + D * i; }
+  static_assert(128 * QT + D * QT <= (int)kTmemCols, "TMEM budget");
+};
+
+template <int QT>
+struct FwdWarps {
+  static constexpr int kSoftmax0 = 0;          // warps [0, 4 QT)
+  static constexpr int kCorrection0 = 4 * QT;  // 4 warps
+  static constexpr int kMma = 4 * QT + 4;
+  static constexpr int kLoad = 4 * QT + 5;
+  static constexpr int kNumWarps = 4 * QT + 8;  // whole warpgroups
+  static constexpr int kThreads = 32 * kNumWarps;
+};
+
+struct Unit {
+  int bh;
+  int q_row0;
+  int n_max;
+};
+
+// Work unit t -> (head, first query row, key-tile counts per query tile).
+// Causal units go longest first (the last query tiles need the most keys).
+// Non-causal units of one head are adjacent, so CTAs running together share
+// that head's K/V in L2.
+template <int QT, bool CAUSAL>
+__device__ __forceinline__ Unit decode_unit(int t, const FwdParams& p,
+                                            int (&n)[QT]) {
+  Unit w;
+  int u;
+  if (CAUSAL) {
+    u = p.n_units - 1 - t / p.BH;
+    w.bh = t % p.BH;
+  } else {
+    u = t % p.n_units;
+    w.bh = t / p.n_units;
+  }
+  w.q_row0 = u * kBM * QT;
+  w.n_max = 0;
+#pragma unroll
+  for (int i = 0; i < QT; ++i) {
+    const int q0 = w.q_row0 + kBM * i;
+    int ni;
+    if (q0 >= p.S)
+      ni = 0;
+    else if (CAUSAL)
+      ni = q0 / kBN + 1;  // tiles up to and including the diagonal
+    else
+      ni = p.n_kv_tiles;
+    n[i] = ni;
+    w.n_max = ni > w.n_max ? ni : w.n_max;
+  }
+  return w;
+}
+
+__device__ __forceinline__ void raise_error(const FwdParams& p,
+                                            volatile int* abort_flag, int code,
+                                            int role, int bar) {
+  if (atomicCAS(p.status, 0, code) == 0) {
+    p.status[1] = (role << 8) | bar;
+    p.status[2] = (int)blockIdx.x;
+  }
+  *abort_flag = 1;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+template <int D, int QT, int NS, bool CAUSAL, bool BF16>
+__global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
+    fattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const FwdParams p) {
+  using L = FwdLayout<D, QT, NS>;
+  using W = FwdWarps<QT>;
+  extern __shared__ uint8_t smem_raw[];
+
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const smem = smem_raw + (base - raw);
+  const uint32_t sQ = base + L::kQ;
+  const uint32_t sKV = base + L::kKV;
+  const uint32_t bars = base + L::kBars;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  float* const sAlpha = reinterpret_cast<float*>(smem + L::kAlpha);
+  float* const sRowL = reinterpret_cast<float*>(smem + L::kRowL);
+  float* const sRowM = reinterpret_cast<float*>(smem + L::kRowM);
+
+  auto bar = [&](int slot) -> uint32_t { return bars + 8u * slot; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint64_t tmo = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < QT; ++i) {
+      ptx::mbar_init(bar(L::bQFull + i), 1);
+      ptx::mbar_init(bar(L::bQEmpty + i), 1);
+      ptx::mbar_init(bar(L::bSFull + i), 1);
+      ptx::mbar_init(bar(L::bPFull + i), kBM);
+      ptx::mbar_init(bar(L::bStats + i), kBM);
+      ptx::mbar_init(bar(L::bOReady + i), kBM);
+      ptx::mbar_init(bar(L::bPVDone + i), 1);
+      ptx::mbar_init(bar(L::bOEmpty + i), kBM);
+    }
+    for (int s = 0; s < NS; ++s) {
+      ptx::mbar_init(bar(L::bKVFull + s), 1);
+      ptx::mbar_init(bar(L::bKVEmpty + s), 1);
+    }
+    ptx::mbar_init(bar(L::bDrain), 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == W::kMma) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == W::kLoad) {
+    // ------------------------------------------------------------ load warp
+    if (lane == 0) {
+      ptx::tma_prefetch_desc(&tm_q);
+      ptx::tma_prefetch_desc(&tm_k);
+      ptx::tma_prefetch_desc(&tm_v);
+      uint32_t kv_idx = 0, kv_ph = 0;
+      int q_uses[QT];
+      for (int i = 0; i < QT; ++i) q_uses[i] = 0;
+      uint32_t kv_filled = 0, kv_fill_ph = 0;  // per stage: ever filled, parity
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
+        int n[QT];
+        const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
+        for (int i = 0; ok && i < QT; ++i) {
+          if (n[i] == 0) continue;
+          if (q_uses[i] > 0 &&
+              !ptx::mbar_wait(bar(L::bQEmpty + i), (q_uses[i] - 1) & 1, abort_flag, tmo)) {
+            raise_error(p, abort_flag, kErrPipelineTimeout, kRoleLoad, L::bQEmpty + i);
+            ok = false;
+            break;
+          }
+          const uint32_t qb = bar(L::bQFull + i);
+          ptx::mbar_arrive_expect_tx(qb, L::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < D / kSwizzleChunkCols; ++c)
+            ptx::tma_load_3d(sQ + i * L::kTileBytes + c * kChunkBytes, &tm_q, qb,
+                             c * kSwizzleChunkCols, w.q_row0 + kBM * i, w.bh);
+          ++q_uses[i];
+        }
+        for (int j = 0; ok && j < w.n_max; ++j) {
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {
+            if (!ptx::mbar_wait(bar(L::bKVEmpty + kv_idx), kv_ph ^ 1u, abort_flag, tmo)) {
+              raise_error(p, abort_flag, kErrPipelineTimeout, kRoleLoad, L::bKVEmpty + kv_idx);
+              ok = false;
+              break;
+            }
+            const uint32_t fb = bar(L::bKVFull + kv_idx);
+            ptx::mbar_arrive_expect_tx(fb, L::kTileBytes);
+#pragma unroll
+            for (int c = 0; c < D / kSwizzleChunkCols; ++c)
+              ptx::tma_load_3d(sKV + kv_idx * L::kTileBytes + c * kChunkBytes,
+                               kv == 0 ? &tm_k : &tm_v, fb, c * kSwizzleChunkCols,
+                               j * kBN, w.bh);
+            kv_filled |= 1u << kv_idx;
+            kv_fill_ph = (kv_fill_ph & ~(1u << kv_idx)) | (kv_ph << kv_idx);
+            if (++kv_idx == NS) {
+              kv_idx = 0;
+              kv_ph ^= 1u;
+            }
+          }
+        }
+      }
+      // Never leave with copies in flight into this CTA's shared memory.
+      for (int s = 0; s < NS; ++s)
+        if (kv_filled & (1u << s))
+          ptx::mbar_wait(bar(L::bKVFull + s), (kv_fill_ph >> s) & 1u, abort_flag, tmo);
+      for (int i = 0; i < QT; ++i)
+        if (q_uses[i] > 0)
+          ptx::mbar_wait(bar(L::bQFull + i), (q_uses[i] - 1) & 1, abort_flag, tmo);
+    }
+  } else if (warp == W::kMma) {
+    // ------------------------------------------------------------- MMA warp
+    if (lane == 0) {
+      constexpr uint32_t kIdS = ptx::idesc_f16(BF16 ? 1 : 0, kBM, kBN, 0, 0);
+      constexpr uint32_t kIdPV = ptx::idesc_f16(BF16 ? 1 : 0, kBM, D, 0, 1);
+      uint32_t kv_idx = 0, kv_ph = 0;
+      int q_uses[QT], p_cnt[QT], or_cnt[QT], oe_cnt[QT], used[QT];
+      for (int i = 0; i < QT; ++i) q_uses[i] = p_cnt[i] = or_cnt[i] = oe_cnt[i] = used[i] = 0;
+      bool ok = true;
+
+      auto wait_or_fail = [&](int slot, uint32_t parity) -> bool {
+        if (ptx::mbar_wait(bar(slot), parity, abort_flag, tmo)) return true;
+        raise_error(p, abort_flag, kErrPipelineTimeout, kRoleMma, slot);
+        return false;
+      };
+      auto next_kv = [&](uint32_t& slot) -> bool {
+        if (!wait_or_fail(L::bKVFull + kv_idx, kv_ph)) return false;
+        slot = kv_idx;
+        if (++kv_idx == NS) {
+          kv_idx = 0;
+          kv_ph ^= 1u;
+        }
+        ptx::tc_fence_after();
+        return true;
+      };
+      // S_i = Q_i K^T: M = 128, N = 128, K = D in steps of 16.
+      auto issue_s = [&](int i, uint32_t k_slot) {
+        const uint32_t d = tmem + L::colS(i);
+        const uint32_t qa = sQ + i * L::kTileBytes;
+        const uint32_t kb = sKV + k_slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * kChunkBytes + (kk % 4) * 32;
+          ptx::mma_ss(d, ptx::smem_desc_sw128(qa + off, 16, 1024),
+                      ptx::smem_desc_sw128(kb + off, 16, 1024), kIdS, kk > 0);
+        }
+      };
+      // O_i += P_i V: M = 128, N = D, K = 128 keys in steps of 16.  P_i is
+      // read from TMEM (two 16-bit values per column); V is MN-major.
+      auto issue_pv = [&](int i, uint32_t v_slot, bool acc) {
+        const uint32_t d = tmem + L::colO(i);
+        const uint32_t vb = sKV + v_slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          ptx::mma_ts(d, tmem + L::colS(i) + kk * 8,
+                      ptx::smem_desc_sw128(vb + kk * 16 * 128, kChunkBytes, 1024),
+                      kIdPV, (acc || kk > 0) ? 1u : 0u);
+      };
+
+      for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
+        int n[QT];
+        const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
+        for (int i = 0; ok && i < QT; ++i)
+          if (n[i] > 0) {
+            ok = wait_or_fail(L::bQFull + i, q_uses[i] & 1);
+            ++q_uses[i];
+          }
+        uint32_t k_slot = 0;
+        if (ok) ok = next_kv(k_slot);
+        if (!ok) break;
+        for (int i = 0; i < QT; ++i)
+          if (n[i] > 0) {
+            issue_s(i, k_slot);
+            ptx::mma_commit(bar(L::bSFull + i));
+            if (n[i] == 1) ptx::mma_commit(bar(L::bQEmpty + i));
+          }
+        ptx::mma_commit(bar(L::bKVEmpty + k_slot));
+
+        for (int j = 0; ok && j < w.n_max; ++j) {
+          uint32_t v_slot = 0, kn_slot = 0;
+          bool have_kn = false;
+          if (!next_kv(v_slot)) {
+            ok = false;
+            break;
+          }
+          int last_pv = -1;
+          for (int i = 0; i < QT; ++i)
+            if (j < n[i]) last_pv = i;
+          for (int i = 0; ok && i < QT; ++i) {
+            if (j < n[i]) {
+              ok = wait_or_fail(L::bPFull + i, p_cnt[i] & 1);
+              ++p_cnt[i];
+              if (ok && j > 0) {
+                ok = wait_or_fail(L::bOReady + i, or_cnt[i] & 1);
+                ++or_cnt[i];
+              } else if (ok && used[i] > 0) {
+                ok = wait_or_fail(L::bOEmpty + i, oe_cnt[i] & 1);
+                ++oe_cnt[i];
+              }
+              if (!ok) break;
+              ptx::tc_fence_after();
+              issue_pv(i, v_slot, j > 0);
+              ptx::mma_commit(bar(L::bPVDone + i));
+              if (i == last_pv) ptx::mma_commit(bar(L::bKVEmpty + v_slot));
+            }
+            if (j + 1 < n[i]) {
+              if (!have_kn) {
+                if (!next_kv(kn_slot)) {
+                  ok = false;
+                  break;
+                }
+                have_kn = true;
+              }
+              issue_s(i, kn_slot);
+              ptx::mma_commit(bar(L::bSFull + i));
+              if (j + 2 == n[i]) ptx::mma_commit(bar(L::bQEmpty + i));
+            }
+          }
+          if (have_kn) ptx::mma_commit(bar(L::bKVEmpty + kn_slot));
+        }
+        for (int i = 0; i < QT; ++i)
+          if (n[i] > 0) ++used[i];
+      }
+      // Drain: every MMA this thread issued completes before TMEM is freed.
+      ptx::mma_commit(bar(L::bDrain));
+      ptx::mbar_wait(bar(L::bDrain), 0, abort_flag, tmo);
+    }
+  } else if (warp < W::kCorrection0) {
+    // ---------------------------------------------------- softmax warpgroups
+    const int i = warp / 4;          // query tile of this warpgroup
+    const int quarter = warp % 4;    // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;
+    const uint32_t s_addr = tmem + ((uint32_t)(quarter * 32) << 16) + L::colS(i);
+    const float c = p.scale_log2;
+    int sf_cnt = 0;
+    for (int t = blockIdx.x; t < p.total_units; t += gridDim.x) {
+      int n[QT];
+      const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
+      const int nk = n[i];
+      if (nk == 0) continue;
+      float m = -INFINITY;  // running max of scaled scores (log2 domain)
+      float l = 0.f;        // running sum of exp2(s*c - m)
+      bool ok = true;
+      for (int j = 0; j < nk; ++j) {
+        ok = ptx::mbar_wait(bar(L::bSFull + i), sf_cnt & 1, abort_flag, tmo);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          if (lane == 0) raise_error(p, abort_flag, kErrPipelineTimeout, kRoleSoftmax, L::bSFull + i);
+          break;
+        }
+        ++sf_cnt;
+        ptx::tc_fence_after();
+        float s[kBN];
+#pragma unroll
+        for (int ch = 0; ch < kBN / 32; ++ch) {
+          uint32_t u[32];
+          ptx::tmem_ld32(s_addr + ch * 32, u);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) s[ch * 32 + e] = __uint_as_float(u[e]);
+        }
+        ptx::tmem_wait_ld();
+        // masks: causal diagonal tile keeps key <= query; keys >= S removed
+        const int kv0 = j * kBN;
+        const bool diag = CAUSAL && (j == nk - 1);
+        const bool ragged = kv0 + kBN > p.S;
+        if (diag || ragged) {
+          int limit = kBN;
+          if (diag) limit = r + 1;
+          if (ragged && p.S - kv0 < limit) limit = p.S - kv0;
+#pragma unroll
+          for (int e = 0; e < kBN; ++e) s[e] = e < limit ? s[e] : -INFINITY;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int e = 1; e < kBN; ++e) mx = fmaxf(mx, s[e]);
+        const float m_new = fmaxf(m, mx * c);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = ex2(m - m_use);
+        if (j > 0) {
+          sAlpha[i * kBM + r] = alpha;
+          ptx::mbar_arrive(bar(L::bStats + i));
+        }
+        const float neg = -m_use;
+        float sum = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < kBN / 32; ++ch) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2(fmaf(s[ch * 32 + 2 * e], c, neg));
+            const float p1 = ex2(fmaf(s[ch * 32 + 2 * e + 1], c, neg));
+            sum += p0 + p1;
+            pk[e] = pack2<BF16>(p0, p1);
+          }
+          ptx::tmem_st16(s_addr + ch * 16, pk);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::bPFull + i));
+        l = alpha * l + sum;
+        m = m_use;
+      }
+      if (!ok) break;
+      sRowL[i * kBM + r] = l;
+      sRowM[i * kBM + r] = m;
+      ptx::mbar_arrive(bar(L::bStats + i));
+    }
+  } else if (warp < W::kMma) {
+    // -------------------------------------------------- correction warpgroup
+    const int quarter = warp % 4;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    int st_cnt[QT], pd_cnt[QT];
+    for (int i = 0; i < QT; ++i) st_cnt[i] = pd_cnt[i] = 0;
+    bool ok = true;
+    auto wait_all = [&](int slot, uint32_t parity) -> bool {
+      bool w_ok = ptx::mbar_wait(bar(slot), parity, abort_flag, tmo);
+      w_ok = __all_sync(0xffffffffu, w_ok);
+      if (!w_ok && lane == 0)
+        raise_error(p, abort_flag, kErrPipelineTimeout, kRoleCorrection, slot);
+      return w_ok;
+    };
+    for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
+      int n[QT];
+      const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
+      for (int j = 1; ok && j < w.n_max; ++j) {
+        for (int i = 0; i < QT; ++i) {
+          if (j >= n[i]) continue;
+          if (!wait_all(L::bStats + i, st_cnt[i] & 1)) { ok = false; break; }
+          ++st_cnt[i];
+          const float a = sAlpha[i * kBM + r];
+          if (!wait_all(L::bPVDone + i, pd_cnt[i] & 1)) { ok = false; break; }
+          ++pd_cnt[i];
+          if (__any_sync(0xffffffffu, a != 1.f)) {
+            ptx::tc_fence_after();
+            const uint32_t o_addr = tmem + lane_off + L::colO(i);
+#pragma unroll
+            for (int ch = 0; ch < D / 32; ++ch) {
+              uint32_t u[32];
+              ptx::tmem_ld32(o_addr + ch * 32, u);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * a);
+              ptx::tmem_st32(o_addr + ch * 32, u);
+            }
+            ptx::tmem_wait_st();
+          }
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::bOReady + i));
+        }
+      }
+      if (!ok) break;
+      // epilogue: O = acc / l (one reciprocal per row), LSE = ln2 (m + log2 l)
+      for (int i = 0; i < QT; ++i) {
+        if (n[i] == 0) continue;
+        if (!wait_all(L::bStats + i, st_cnt[i] & 1)) { ok = false; break; }
+        ++st_cnt[i];
+        const float l = sRowL[i * kBM + r];
+        const float m = sRowM[i * kBM + r];
+        if (!wait_all(L::bPVDone + i, pd_cnt[i] & 1)) { ok = false; break; }
+        ++pd_cnt[i];
+        ptx::tc_fence_after();
+        const float inv_l = 1.0f / l;
+        const int row = w.q_row0 + kBM * i + r;
+        const bool valid = row < p.S;
+        const size_t grow = (size_t)w.bh * (size_t)p.S + (size_t)row;
+        uint4* const orow = reinterpret_cast<uint4*>(
+            reinterpret_cast<uint8_t*>(p.o) + grow * (size_t)(D * 2));
+        const uint32_t o_addr = tmem + lane_off + L::colO(i);
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t u[32];
+          ptx::tmem_ld32(o_addr + ch * 32, u);
+          ptx::tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack2<BF16>(__uint_as_float(u[2 * e]) * inv_l,
+                                __uint_as_float(u[2 * e + 1]) * inv_l);
+          if (valid) {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              orow[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+        if (valid) p.lse[grow] = (m + log2f(l)) * 0.69314718055994531f;
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::bOEmpty + i));
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == W::kMma) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace fattn

@@ -1,0 +1,71 @@
+// Per-head-dim kernel configuration and the launcher shared by the
+// instantiation units (fattn_fwd_d64.cu, fattn_fwd_d128.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fattn_kernel.cuh"
+
+namespace fattn {
+
+// Query tiles per work unit and K/V ring depth, chosen so shared memory stays
+// under the 227 KB a CTA may use (one CTA per SM).
+template <int D>
+struct FwdConfig;
+template <>
+struct FwdConfig<64> {
+  static constexpr int QT = 1;
+  static constexpr int NS = 8;
+};
+template <>
+struct FwdConfig<128> {
+  static constexpr int QT = 1;
+  static constexpr int NS = 5;
+};
+
+struct LaunchArgs {
+  const CUtensorMap* tm_q;
+  const CUtensorMap* tm_k;
+  const CUtensorMap* tm_v;
+  FwdParams params;
+  int grid;
+  cudaStream_t stream;
+};
+
+template <int D>
+struct FwdShape {
+  using C = FwdConfig<D>;
+  using L = FwdLayout<D, C::QT, C::NS>;
+  static constexpr int kSmem = L::kSmemBytes;
+  static constexpr int kThreads = FwdWarps<C::QT>::kThreads;
+  static_assert(kSmem <= 232448, "shared memory per CTA");
+};
+
+template <int D, bool CAUSAL, bool BF16>
+cudaError_t launch_fwd(const LaunchArgs& a) {
+  using C = FwdConfig<D>;
+  auto kern = &fattn_fwd_kernel<D, C::QT, C::NS, CAUSAL, BF16>;
+  constexpr int smem = FwdShape<D>::kSmem;
+  // The shared-memory opt-in is per function and device; remember it for the
+  // first 64 devices (setting it twice is harmless).
+  static volatile bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             smem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set[dev] = true;
+  }
+  kern<<<a.grid, FwdShape<D>::kThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k,
+                                                          *a.tm_v, a.params);
+  return cudaGetLastError();
+}
+
+// Defined in the instantiation units.
+cudaError_t launch_fwd_d64(bool causal, bool bf16, const LaunchArgs& a);
+cudaError_t launch_fwd_d128(bool causal, bool bf16, const LaunchArgs& a);
+
+}  // namespace fattn

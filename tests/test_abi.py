@@ -1,0 +1,91 @@
+"""The C-ABI library: it loads without a GPU, exports every entry point that
+include/fattn.h declares, and rejects bad arguments on the host before any
+CUDA call (so these run on a CPU-only machine)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_forward_10_gb300 as fattn
+from exact_attention_forward_10_gb300 import build as fbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fbuild.build()
+    return fattn.lib()
+
+
+def declared_symbols():
+    out = []
+    for name in os.listdir(os.path.join(ROOT, "include")):
+        if not name.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", name)).read()
+        out += re.findall(r"^FATTN_API\s[^;(]*?\b(\w+)\s*\(", text, re.M)
+    return sorted(set(out))
+
+
+def test_header_declares_entry_points():
+    syms = declared_symbols()
+    assert "fattn_fwd" in syms and "fattn_last_error" in syms
+    assert len(syms) >= 5
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for s in declared_symbols():
+        assert hasattr(lib, s), f"{s} declared in include/ but not exported"
+
+
+def test_version_and_strings(lib):
+    assert fattn.fattn_version() >= 100
+    for code in range(-7, 1):
+        assert fattn.fattn_error_string(code) not in ("", "unknown status")
+    assert fattn.fattn_error_string(-99) == "unknown status"
+
+
+# A fake, 16-byte aligned, non-null address: host checks must reject the call
+# before the pointer is ever looked at.
+P = 1 << 20
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(q=0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(lse=0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(B=0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(S=-3), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(D=96), fattn.FATTN_ERR_UNSUPPORTED),
+    (dict(D=256), fattn.FATTN_ERR_UNSUPPORTED),
+    (dict(dtype=2), fattn.FATTN_ERR_UNSUPPORTED),
+    (dict(q=P + 8), fattn.FATTN_ERR_MISALIGNED),
+    (dict(o=P * 9 + 2), fattn.FATTN_ERR_MISALIGNED),
+    (dict(lse=P * 11 + 2), fattn.FATTN_ERR_MISALIGNED),
+    (dict(B=1 << 16, H=1 << 10, S=1 << 10), fattn.FATTN_ERR_TOO_LARGE),
+    (dict(o=P), fattn.FATTN_ERR_INVALID_ARG),          # o aliases q
+    (dict(lse=P * 7 + 64), fattn.FATTN_ERR_INVALID_ARG),  # lse inside v
+])
+def test_host_side_rejections(lib, args, want):
+    a = dict(q=P, k=P * 3, v=P * 7, o=P * 9, lse=P * 11, B=1, H=2, S=128,
+             D=64, causal=0, scale=0.125, dtype=0, stream=0)
+    a.update(args)
+    rc = fattn.fattn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"],
+                         a["H"], a["S"], a["D"], a["causal"], a["scale"],
+                         a["dtype"], a["stream"])
+    assert rc == want
+
+
+def test_plan_without_device(lib):
+    p = fattn.fattn_plan(2, 16, 8192, 128, True)
+    assert p["q_tiles_per_unit"] in (1, 2)
+    assert p["units"] == 2 * 16 * (8192 // (128 * p["q_tiles_per_unit"]))
+    assert p["smem_bytes"] <= 232448
+    assert p["block"] % 128 == 0
+    assert 1 <= p["grid"] <= p["units"]
+    with pytest.raises(fattn.FattnError):
+        fattn.fattn_plan(1, 1, 10, 80)

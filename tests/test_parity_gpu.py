@@ -1,0 +1,118 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Small and ragged shapes are compared on every element; the full-size
+workloads (the benchmark shapes, in the launch configuration the benchmark
+times) on sampled rows.  Output buffers are NaN-poisoned first, so an
+unwritten element fails.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import attn_inputs
+from parity import check_full, check_sampled, run_cuda, compare
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def test_tiny_matches_golden_fixture():
+    with open(os.path.join(HERE, "golden", "tiny_fp16_noncausal_oracle.json")) as f:
+        g = json.load(f)
+    w = attn_inputs.WORKLOADS["tiny"]
+    x = w.inputs()
+    o, lse = run_cuda(x, False)
+    np.testing.assert_allclose(lse.reshape(-1), g["lse"], rtol=0, atol=1e-3)
+    flat = o.reshape(-1, w.D)
+    for r, vals in g["o_rows"].items():
+        np.testing.assert_allclose(flat[int(r)], vals, rtol=0, atol=2e-3)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("S", [1, 2, 127, 128, 129, 255, 300, 513])
+def test_small_and_ragged(S, D, dtype, causal):
+    x = attn_inputs.make_qkv(1, 2, S, D, dtype, seed=1000 + S + D)
+    check_full(x, causal, f"S{S} D{D} {dtype} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_multi_head_multi_tile(D, causal):
+    x = attn_inputs.make_qkv(2, 3, 1000, D, "bf16", seed=7)
+    check_full(x, causal, f"B2 H3 S1000 D{D} causal={causal}")
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_stress_large_scores(dtype):
+    """Q, K x 4: score std ~16, so the running max moves a lot."""
+    x = attn_inputs.make_qkv(1, 4, 777, 128, dtype, seed=9, qk_mult=4.0)
+    for causal in (False, True):
+        check_full(x, causal, f"x4 {dtype} causal={causal}")
+
+
+def test_config_tiny():
+    w = attn_inputs.WORKLOADS["tiny"]
+    check_full(w.inputs(), False, w.name)
+
+
+@pytest.mark.parametrize("key", ["s2048_d64", "s2048_d128"])
+def test_config_s2048_full(key):
+    w = attn_inputs.WORKLOADS[key]
+    x = w.inputs()
+    for causal in w.causal:
+        check_full(x, causal, f"{w.name} causal={causal}")
+
+
+@pytest.mark.parametrize("key", ["s8192_d128", "s8192_d128_x4"])
+def test_config_s8192_sampled(key):
+    w = attn_inputs.WORKLOADS[key]
+    x = w.inputs()
+    for causal in w.causal:
+        check_sampled(x, causal, seed=w.seed, label=f"{w.name} causal={causal}")
+
+
+@pytest.mark.parametrize("w", attn_inputs.sweep_workloads(), ids=lambda w: w.name)
+def test_sweep_sampled(w):
+    x = w.inputs()
+    for causal in w.causal:
+        check_sampled(x, causal, seed=w.seed, label=f"{w.name} causal={causal}",
+                      stride=64, n_heads=2)
+
+
+def test_many_heads_short_sequences():
+    x = attn_inputs.make_qkv(8, 64, 256, 64, "fp16", seed=11)
+    for causal in (False, True):
+        check_sampled(x, causal, seed=11, label=f"B8 H64 S256 causal={causal}",
+                      n_heads=6)
+
+
+def test_scale_argument():
+    x = attn_inputs.make_qkv(1, 2, 200, 64, "fp16", seed=12)
+    import oracle
+    for scale in (0.05, 0.3):
+        o, lse = run_cuda(x, True, scale=scale)
+        ro, rl = oracle.attn_fwd(x.q, x.k, x.v, True, scale)
+        compare(o, lse, ro, rl, "fp16", f"scale={scale}")
+
+
+def test_repeated_calls_are_deterministic():
+    x = attn_inputs.make_qkv(2, 4, 640, 128, "bf16", seed=13)
+    o1, l1 = run_cuda(x, True)
+    o2, l2 = run_cuda(x, True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
