@@ -1,0 +1,425 @@
+"""Attention-forward benchmark: TFLOPS (4 B H S^2 D, halved when causal).
+
+One step is one pass of the whole path over one batch: the non-causal and the
+causal forward of the B=2, H=16, S=8192, D=128 bf16 workload (seed 3), each a
+single fattn_fwd launch through the C ABI.  Inputs (192 MiB Q, K, V) and
+outputs are larger than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs under torchrun: every rank runs the same per-GPU workload (weak
+scaling, no collective on the data path); the timing is the max over ranks.
+``--impl reference`` times the fp64 CPU oracle on a bounded row sample of the
+same workload (the reference arm: this path has no other implementation).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import attn_inputs  # noqa: E402
+
+METRIC = ("attn fwd TFLOPS (4BHS²D, ½ if causal) and % of GB300 dense "
+          "16-bit tensor peak")
+UNIT = "TFLOP/s"
+WORKLOAD = attn_inputs.WORKLOADS["s8192_d128"]
+MASKS = (False, True)
+
+
+def metric_flops(B, H, S, D, causal) -> float:
+    f = 4.0 * B * H * S * S * D
+    return f / 2 if causal else f
+
+
+def row_flops(S, D, causal) -> float:
+    """The metric's FLOPs per query row (causal: the halved average)."""
+    return (2.0 if causal else 4.0) * S * D
+
+
+def workload_config(w, extra=None) -> dict:
+    c = {"workload": f"B{w.B} H{w.H} S{w.S} D{w.D} {w.dtype}, non-causal + "
+                     f"causal, Q/K/V iid N(0,1) seed {w.seed}, scale 1/sqrt(D)",
+         "B": w.B, "H": w.H, "S": w.S, "D": w.D, "masks": "non-causal+causal",
+         "l2": "inputs larger than L2 (Q,K,V 192 MiB + O 64 MiB per launch); "
+               "no flush"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def load_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"burst": float(d["bf16_tflops"]),
+                "sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"burst": 1900.0, "sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------ reference arm
+
+def oracle_sample_rows(w, n_rows: int, seed: int) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(w.B * w.H * w.S, size=n_rows, replace=False))
+
+
+def cpu_oracle_run(x, w, rows_per_mask: int, seed: int):
+    """Oracle on ``rows_per_mask`` sampled rows per mask; returns (seconds,
+    metric FLOPs of those rows, threads)."""
+    import oracle
+    threads = oracle.default_threads()
+    flops = 0.0
+    t0 = time.perf_counter()
+    for m, causal in enumerate(MASKS):
+        rows = oracle_sample_rows(w, rows_per_mask, seed + m)
+        oracle.attn_fwd(x.q, x.k, x.v, causal, w.scale, rows=rows, threads=threads)
+        flops += rows_per_mask * row_flops(w.S, w.D, causal)
+    return time.perf_counter() - t0, flops, threads
+
+
+def calibrate_rows(x, w, target_s: float) -> int:
+    """Rows per mask so that one oracle sample takes about ``target_s``."""
+    n = 64
+    dt, _, _ = cpu_oracle_run(x, w, n, 999)
+    while dt < 0.5 and n < (1 << 16):
+        n *= 4
+        dt, _, _ = cpu_oracle_run(x, w, n, 999)
+    return max(16, int(n * target_s / max(dt, 1e-6)))
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = WORKLOAD
+    x = w.inputs()
+    rows = calibrate_rows(x, w, target_s=max(0.2, min(10.0, 90.0 / max(1, args.steps + args.warmup))))
+    for i in range(args.warmup):
+        cpu_oracle_run(x, w, rows, 100 + i)
+    times, flops = [], 0.0
+    threads = 1
+    for i in range(args.steps):
+        dt, fl, threads = cpu_oracle_run(x, w, rows, 1000 + i)
+        times.append(dt)
+        flops += fl
+    total = sum(times)
+    value = flops / total / 1e12
+    sample = (f"{rows} sampled query rows per mask per step (of {w.B * w.H * w.S}); "
+              f"metric FLOPs of those rows / wall time")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * total / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, {"parallelism": "host cores, rank 0 only"}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_fattn(args):
+    import torch
+
+    import exact_attention_forward_10_gb300 as fattn
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = WORKLOAD
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    x = w.inputs()
+    host = [torch.from_numpy(a).to(tdt).pin_memory() for a in (x.q, x.k, x.v)]
+    q, k, v = (h.to(dev) for h in host)
+    B, H, S, D = w.B, w.H, w.S, w.D
+    outs = {c: (torch.empty_like(q), torch.empty((B, H, S), dtype=torch.float32, device=dev))
+            for c in MASKS}
+    stream = torch.cuda.Stream(dev)
+    sptr = stream.cuda_stream
+    code = fattn.FATTN_BF16 if w.dtype == "bf16" else fattn.FATTN_FP16
+
+    def launch(causal, qq, kk, vv):
+        o, l = outs[causal]
+        rc = fattn.fattn_fwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
+                             l.data_ptr(), B, H, S, D, causal, w.scale, code, sptr)
+        if rc != 0:
+            raise fattn.FattnError(rc)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # correctness gate before timing: no kernel error
+    with torch.cuda.stream(stream):
+        for c in MASKS:
+            launch(c, q, k, v)
+    rc, where = fattn.fattn_last_error(sptr)
+    if rc != 0:
+        raise RuntimeError(f"kernel status {rc} at {where}")
+
+    # ---- device-timed region: inputs resident in HBM
+    n_ev = args.steps * len(MASKS)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n_ev)]
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            for c in MASKS:
+                launch(c, q, k, v)
+    barrier()
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.25)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        e = 0
+        for _ in range(args.steps):
+            for c in MASKS:
+                ev[e][0].record(stream)
+                launch(c, q, k, v)
+                ev[e][1].record(stream)
+                e += 1
+        t_end.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    per_launch = {c: [] for c in MASKS}
+    for i, (a, b) in enumerate(ev):
+        per_launch[MASKS[i % len(MASKS)]].append(a.elapsed_time(b))
+    rc, where = fattn.fattn_last_error(sptr)
+    if rc != 0:
+        raise RuntimeError(f"kernel status {rc} at {where}")
+
+    # ---- end to end through the public call, host buffers
+    h_outs = {c: (torch.empty((B, H, S, D), dtype=tdt).pin_memory(),
+                  torch.empty((B, H, S), dtype=torch.float32).pin_memory()) for c in MASKS}
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        qq, kk, vv = (h.to(dev, non_blocking=True) for h in host)
+        for c in MASKS:
+            launch(c, qq, kk, vv)
+        for c in MASKS:
+            h_outs[c][0].copy_(outs[c][0], non_blocking=True)
+            h_outs[c][1].copy_(outs[c][1], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(h.numel() * h.element_size() for h in host)
+    d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size()
+              for o, l in h_outs.values())
+
+    # ---- max over ranks
+    step_ms = elapsed_ms / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([step_ms, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, e2e_ms = float(t[0]), float(t[1])
+
+    flops_step = sum(metric_flops(B, H, S, D, c) for c in MASKS)
+    value = world * flops_step / (step_ms * 1e-3) / 1e12
+    e2e_value = world * flops_step / (e2e_ms * 1e-3) / 1e12
+    peaks = load_peaks()
+    per_mask = {}
+    for c in MASKS:
+        ms = statistics.median(per_launch[c])
+        tf = metric_flops(B, H, S, D, c) / (ms * 1e-3) / 1e12
+        per_mask["causal" if c else "noncausal"] = {
+            "ms_median": ms, "tflops": tf, "frac_of_measured_burst": tf / peaks["burst"]}
+    # dominant kernel: the non-causal launch (2/3 of the step's FLOPs)
+    dom_ms = statistics.mean(per_launch[False])
+    achieved = metric_flops(B, H, S, D, False) / (dom_ms * 1e-3) / 1e12
+    traffic = load_traffic()
+    plan = fattn.fattn_plan(B, H, S, D, False)
+
+    result = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(x, w)
+        result = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": workload_config(w, {"parallelism": f"replicas x{world}",
+                                          "grid": plan["grid"], "block": plan["block"],
+                                          "units_per_launch": plan["units"]}),
+            "per_mask": per_mask,
+            "roofline": {"bound": "tensor", "achieved": achieved,
+                         "peak": peaks["burst"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["burst"],
+                         "peak_kind": f"bf16 dense, {peaks['source']} burst",
+                         "kernel": "fattn_fwd_kernel<D=128, non-causal, bf16>",
+                         "traffic": traffic},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * len(MASKS),
+            "clocks": clocks,
+        }
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources; ties a stored ncu traffic figure to the kernel
+    it was measured on."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "exact_attention_forward_10_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """DRAM bytes (read + write) per launch of the dominant kernel from the
+    committed ncu summary; None when there is none for the current sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f).get("fattn_fwd_noncausal_bf16_d128")
+    if not d or d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("bytes_per_launch")
+
+
+def cpu_baseline(x, w) -> dict:
+    rows = calibrate_rows(x, w, target_s=15.0)
+    dt, fl, threads = cpu_oracle_run(x, w, rows, 4242)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": f"{rows} sampled query rows per mask of {w.name} "
+                      f"({dt:.1f} s); metric FLOPs of those rows / wall time"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="fattn", choices=["fattn", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_fattn(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
