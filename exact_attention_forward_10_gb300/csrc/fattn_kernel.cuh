@@ -100,6 +100,15 @@ struct FwdWarps {
   static constexpr int kLoad = 4 * QT + 5;
   static constexpr int kNumWarps = 4 * QT + 8;  // whole warpgroups
   static constexpr int kThreads = 32 * kNumWarps;
+  // Registers per thread after the per-warpgroup split (QT == 2 only): the
+  // softmax warpgroups hold a 128-float score row; the shares add up to the
+  // 128 per thread the 512-thread block is launched with.
+  static constexpr int kRegSoftmax = 160;
+  static constexpr int kRegCorrection = 96;
+  static constexpr int kRegOther = 96;
+  static_assert(QT != 2 || 2 * kRegSoftmax + kRegCorrection + kRegOther ==
+                               4 * (65536 / kThreads),
+                "register split must equal the launch allocation");
 };
 
 struct Unit {
@@ -140,6 +149,16 @@ __device__ __forceinline__ Unit decode_unit(int t, const FwdParams& p,
     w.n_max = ni > w.n_max ? ni : w.n_max;
   }
   return w;
+}
+
+// Round k of the persistent loop: CTA g takes unit k*G + g in even rounds and
+// k*G + (G-1-g) in odd rounds (a snake over the longest-first order), which
+// evens out the causal work per CTA.  Returns a value >= total when this CTA
+// has nothing in round k.
+__device__ __forceinline__ int unit_of_round(int k) {
+  const int G = (int)gridDim.x;
+  const int g = (int)blockIdx.x;
+  return k * G + ((k & 1) ? (G - 1 - g) : g);
 }
 
 __device__ __forceinline__ void raise_error(const FwdParams& p,
@@ -225,6 +244,12 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // The register split is stated at the top of each role's branch so it
+  // dominates that role's code.
+  if (warp >= W::kMma) {
+    if constexpr (QT == 2) ptx::setmaxnreg_dec<W::kRegOther>();
+  }
+
   if (warp == W::kLoad) {
     // ------------------------------------------------------------ load warp
     if (lane == 0) {
@@ -236,7 +261,9 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       for (int i = 0; i < QT; ++i) q_uses[i] = 0;
       uint32_t kv_filled = 0, kv_fill_ph = 0;  // per stage: ever filled, parity
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
+      for (int k = 0; ok && k * (int)gridDim.x < p.total_units; ++k) {
+        const int t = unit_of_round(k);
+        if (t >= p.total_units) continue;
         int n[QT];
         const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
         for (int i = 0; ok && i < QT; ++i) {
@@ -336,7 +363,9 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                       kIdPV, (acc || kk > 0) ? 1u : 0u);
       };
 
-      for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
+      for (int k = 0; ok && k * (int)gridDim.x < p.total_units; ++k) {
+        const int t = unit_of_round(k);
+        if (t >= p.total_units) continue;
         int n[QT];
         const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
         for (int i = 0; ok && i < QT; ++i)
@@ -406,13 +435,16 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
     }
   } else if (warp < W::kCorrection0) {
     // ---------------------------------------------------- softmax warpgroups
+    if constexpr (QT == 2) ptx::setmaxnreg_inc<W::kRegSoftmax>();
     const int i = warp / 4;          // query tile of this warpgroup
     const int quarter = warp % 4;    // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
     const uint32_t s_addr = tmem + ((uint32_t)(quarter * 32) << 16) + L::colS(i);
     const float c = p.scale_log2;
     int sf_cnt = 0;
-    for (int t = blockIdx.x; t < p.total_units; t += gridDim.x) {
+    for (int k = 0; k * (int)gridDim.x < p.total_units; ++k) {
+      const int t = unit_of_round(k);
+      if (t >= p.total_units) continue;
       int n[QT];
       const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
       const int nk = n[i];
@@ -486,6 +518,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
     }
   } else if (warp < W::kMma) {
     // -------------------------------------------------- correction warpgroup
+    if constexpr (QT == 2) ptx::setmaxnreg_dec<W::kRegCorrection>();
     const int quarter = warp % 4;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -499,7 +532,9 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         raise_error(p, abort_flag, kErrPipelineTimeout, kRoleCorrection, slot);
       return w_ok;
     };
-    for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
+    for (int k = 0; ok && k * (int)gridDim.x < p.total_units; ++k) {
+      const int t = unit_of_round(k);
+      if (t >= p.total_units) continue;
       int n[QT];
       const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
       for (int j = 1; ok && j < w.n_max; ++j) {

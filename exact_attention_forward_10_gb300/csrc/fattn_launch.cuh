@@ -15,13 +15,13 @@ template <int D>
 struct FwdConfig;
 template <>
 struct FwdConfig<64> {
-  static constexpr int QT = 1;
+  static constexpr int QT = 2;
   static constexpr int NS = 8;
 };
 template <>
 struct FwdConfig<128> {
-  static constexpr int QT = 1;
-  static constexpr int NS = 5;
+  static constexpr int QT = 2;
+  static constexpr int NS = 4;
 };
 
 struct LaunchArgs {
