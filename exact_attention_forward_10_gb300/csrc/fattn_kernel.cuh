@@ -39,6 +39,13 @@
 #include "fattn_status.h"
 #include "ptx.cuh"
 
+// Optional timeline hook: FATTN_TRACE_EV(round, kv_tile, event) records one
+// event of the pipeline when an instrumented build defines it; the product
+// build compiles it to nothing.
+#ifndef FATTN_TRACE_EV
+#define FATTN_TRACE_EV(round, kv_tile, event) ((void)0)
+#endif
+
 namespace fattn {
 
 constexpr int kBM = 128;  // query rows per tile (one TMEM lane each)
@@ -169,6 +176,13 @@ __device__ __forceinline__ void raise_error(const FwdParams& p,
     p.status[2] = (int)blockIdx.x;
   }
   *abort_flag = 1;
+}
+
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -339,28 +353,42 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         ptx::tc_fence_after();
         return true;
       };
-      // S_i = Q_i K^T: M = 128, N = 128, K = D in steps of 16.
+      // Descriptors: one constant high word (SBO = 1024: eight 128-byte rows
+      // per swizzle atom) and low words stepped by immediates.
+      constexpr uint32_t kHi = ptx::desc_sw128_hi(1024);
+      constexpr uint32_t kTileLo = L::kTileBytes >> 4;  // one K/V stage
+      const uint32_t q_lo = ptx::desc_sw128_lo(sQ, 16);
+      const uint32_t k_lo = ptx::desc_sw128_lo(sKV, 16);
+      const uint32_t v_lo = ptx::desc_sw128_lo(sKV, kChunkBytes);  // LBO: next 64 columns
+      // S_i = Q_i K^T: M = 128, N = 128, K = D in steps of 16 (32 bytes of a
+      // 128-byte swizzled row; the next 64 columns are one chunk further).
       auto issue_s = [&](int i, uint32_t k_slot) {
         const uint32_t d = tmem + L::colS(i);
-        const uint32_t qa = sQ + i * L::kTileBytes;
-        const uint32_t kb = sKV + k_slot * L::kTileBytes;
+        const uint32_t qa = q_lo + i * kTileLo;
+        const uint32_t kb = k_lo + k_slot * kTileLo;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * kChunkBytes + (kk % 4) * 32;
-          ptx::mma_ss(d, ptx::smem_desc_sw128(qa + off, 16, 1024),
-                      ptx::smem_desc_sw128(kb + off, 16, 1024), kIdS, kk > 0);
+          const uint32_t off = ((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4;
+          if (kk == 0)
+            ptx::mma_ss_lohi<0>(d, qa + off, kb + off, kHi, kIdS, 0u);
+          else
+            ptx::mma_ss_lohi<1>(d, qa + off, kb + off, kHi, kIdS, 1u);
         }
       };
       // O_i += P_i V: M = 128, N = D, K = 128 keys in steps of 16.  P_i is
-      // read from TMEM (two 16-bit values per column); V is MN-major.
+      // read from TMEM (two 16-bit values per column); V is MN-major, each
+      // step 16 key rows (2048 bytes) further.
       auto issue_pv = [&](int i, uint32_t v_slot, bool acc) {
         const uint32_t d = tmem + L::colO(i);
-        const uint32_t vb = sKV + v_slot * L::kTileBytes;
+        const uint32_t a = tmem + L::colS(i);
+        const uint32_t vb = v_lo + v_slot * kTileLo;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          ptx::mma_ts(d, tmem + L::colS(i) + kk * 8,
-                      ptx::smem_desc_sw128(vb + kk * 16 * 128, kChunkBytes, 1024),
-                      kIdPV, (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          if (kk == 0)
+            ptx::mma_ts_lohi<0>(d, a, vb, kHi, kIdPV, acc ? 1u : 0u);
+          else
+            ptx::mma_ts_lohi<1>(d, a + kk * 8, vb + kk * (2048 >> 4), kHi, kIdPV, 1u);
+        }
       };
 
       for (int k = 0; ok && k * (int)gridDim.x < p.total_units; ++k) {
@@ -391,6 +419,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
             ok = false;
             break;
           }
+          FATTN_TRACE_EV(k, j, 24);
           int last_pv = -1;
           for (int i = 0; i < QT; ++i)
             if (j < n[i]) last_pv = i;
@@ -406,6 +435,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                 ++oe_cnt[i];
               }
               if (!ok) break;
+              FATTN_TRACE_EV(k, j, 25 + 2 * i);
               ptx::tc_fence_after();
               issue_pv(i, v_slot, j > 0);
               ptx::mma_commit(bar(L::bPVDone + i));
@@ -419,6 +449,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                 }
                 have_kn = true;
               }
+              FATTN_TRACE_EV(k, j, 26 + 2 * i);
               issue_s(i, kn_slot);
               ptx::mma_commit(bar(L::bSFull + i));
               if (j + 2 == n[i]) ptx::mma_commit(bar(L::bQEmpty + i));
@@ -453,6 +484,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       float l = 0.f;        // running sum of exp2(s*c - m)
       bool ok = true;
       for (int j = 0; j < nk; ++j) {
+        FATTN_TRACE_EV(k, j, 8 * i + 0);
         ok = ptx::mbar_wait(bar(L::bSFull + i), sf_cnt & 1, abort_flag, tmo);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
@@ -460,6 +492,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           break;
         }
         ++sf_cnt;
+        FATTN_TRACE_EV(k, j, 8 * i + 1);
         ptx::tc_fence_after();
         float s[kBN];
 #pragma unroll
@@ -470,6 +503,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           for (int e = 0; e < 32; ++e) s[ch * 32 + e] = __uint_as_float(u[e]);
         }
         ptx::tmem_wait_ld();
+        FATTN_TRACE_EV(k, j, 8 * i + 2);
         // masks: causal diagonal tile keeps key <= query; keys >= S removed
         const int kv0 = j * kBN;
         const bool diag = CAUSAL && (j == nk - 1);
@@ -481,33 +515,53 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < kBN; ++e) s[e] = e < limit ? s[e] : -INFINITY;
         }
-        float mx = s[0];
+        // row max: 8 independent chains of 3-input maxima, then combined
+        float acc[8];
 #pragma unroll
-        for (int e = 1; e < kBN; ++e) mx = fmaxf(mx, s[e]);
+        for (int a = 0; a < 8; ++a) acc[a] = fmax3(s[2 * a], s[2 * a + 1], -INFINITY);
+#pragma unroll
+        for (int e = 16; e < kBN; e += 16) {
+#pragma unroll
+          for (int a = 0; a < 8; ++a) acc[a] = fmax3(acc[a], s[e + 2 * a], s[e + 2 * a + 1]);
+        }
+        const float mx = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
+                               fmaxf(acc[6], acc[7]));
         const float m_new = fmaxf(m, mx * c);
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = ex2(m - m_use);
+        FATTN_TRACE_EV(k, j, 8 * i + 3);
         if (j > 0) {
           sAlpha[i * kBM + r] = alpha;
           ptx::mbar_arrive(bar(L::bStats + i));
         }
-        const float neg = -m_use;
-        float sum = 0.f;
+        // p = exp2(s*c - m) with the scale folded into one packed FFMA per
+        // pair; the row sum runs in four packed partial sums
+        const float2 c2 = make_float2(c, c);
+        const float2 neg2 = make_float2(-m_use, -m_use);
+        float2 sum2[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) sum2[a] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int ch = 0; ch < kBN / 32; ++ch) {
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2(fmaf(s[ch * 32 + 2 * e], c, neg));
-            const float p1 = ex2(fmaf(s[ch * 32 + 2 * e + 1], c, neg));
-            sum += p0 + p1;
-            pk[e] = pack2<BF16>(p0, p1);
+            const float2 x = __ffma2_rn(make_float2(s[ch * 32 + 2 * e], s[ch * 32 + 2 * e + 1]),
+                                        c2, neg2);
+            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+            sum2[e & 3] = __fadd2_rn(sum2[e & 3], pp);
+            pk[e] = pack2<BF16>(pp.x, pp.y);
           }
           ptx::tmem_st16(s_addr + ch * 16, pk);
         }
+        const float2 s01 = __fadd2_rn(sum2[0], sum2[1]);
+        const float2 s23 = __fadd2_rn(sum2[2], sum2[3]);
+        const float2 s4 = __fadd2_rn(s01, s23);
+        const float sum = s4.x + s4.y;
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::bPFull + i));
+        FATTN_TRACE_EV(k, j, 8 * i + 4);
         l = alpha * l + sum;
         m = m_use;
       }
@@ -540,11 +594,14 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       for (int j = 1; ok && j < w.n_max; ++j) {
         for (int i = 0; i < QT; ++i) {
           if (j >= n[i]) continue;
+          FATTN_TRACE_EV(k, j, 16 + 4 * i + 0);
           if (!wait_all(L::bStats + i, st_cnt[i] & 1)) { ok = false; break; }
           ++st_cnt[i];
+          FATTN_TRACE_EV(k, j, 16 + 4 * i + 1);
           const float a = sAlpha[i * kBM + r];
           if (!wait_all(L::bPVDone + i, pd_cnt[i] & 1)) { ok = false; break; }
           ++pd_cnt[i];
+          FATTN_TRACE_EV(k, j, 16 + 4 * i + 2);
           if (__any_sync(0xffffffffu, a != 1.f)) {
             ptx::tc_fence_after();
             const uint32_t o_addr = tmem + lane_off + L::colO(i);
@@ -561,6 +618,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           }
           ptx::tc_fence_before();
           ptx::mbar_arrive(bar(L::bOReady + i));
+          FATTN_TRACE_EV(k, j, 16 + 4 * i + 3);
         }
       }
       if (!ok) break;
