@@ -330,7 +330,12 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
     }
   } else if (warp == W::kMma) {
     // ------------------------------------------------------------- MMA warp
-    if (lane == 0) {
+    // The whole warp runs this role converged, so its counters and
+    // descriptors stay warp-uniform; one elected lane issues each tcgen05
+    // instruction.  The issuing thread stalls until the tensor pipe accepts
+    // an MMA, so everything it does between two MMA groups is tensor idle
+    // time: that path is kept short.
+    {
       constexpr uint32_t kIdS = ptx::idesc_f16(BF16 ? 1 : 0, kBM, kBN, 0, 0);
       constexpr uint32_t kIdPV = ptx::idesc_f16(BF16 ? 1 : 0, kBM, D, 0, 1);
       uint32_t kv_idx = 0, kv_ph = 0;
@@ -339,9 +344,13 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       bool ok = true;
 
       auto wait_or_fail = [&](int slot, uint32_t parity) -> bool {
-        if (ptx::mbar_wait(bar(slot), parity, abort_flag, tmo)) return true;
-        raise_error(p, abort_flag, kErrPipelineTimeout, kRoleMma, slot);
-        return false;
+        bool w_ok = ptx::mbar_wait(bar(slot), parity, abort_flag, tmo);
+        w_ok = __all_sync(0xffffffffu, w_ok);
+        if (!w_ok && lane == 0) raise_error(p, abort_flag, kErrPipelineTimeout, kRoleMma, slot);
+        return w_ok;
+      };
+      auto commit = [&](int slot) {
+        if (ptx::elect_one()) ptx::mma_commit(bar(slot));
       };
       auto next_kv = [&](uint32_t& slot) -> bool {
         if (!wait_or_fail(L::bKVFull + kv_idx, kv_ph)) return false;
@@ -366,6 +375,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         const uint32_t d = tmem + L::colS(i);
         const uint32_t qa = q_lo + i * kTileLo;
         const uint32_t kb = k_lo + k_slot * kTileLo;
+        if (!ptx::elect_one()) return;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4;
@@ -382,6 +392,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         const uint32_t d = tmem + L::colO(i);
         const uint32_t a = tmem + L::colS(i);
         const uint32_t vb = v_lo + v_slot * kTileLo;
+        if (!ptx::elect_one()) return;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           if (kk == 0)
@@ -407,10 +418,10 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         for (int i = 0; i < QT; ++i)
           if (n[i] > 0) {
             issue_s(i, k_slot);
-            ptx::mma_commit(bar(L::bSFull + i));
-            if (n[i] == 1) ptx::mma_commit(bar(L::bQEmpty + i));
+            commit(L::bSFull + i);
+            if (n[i] == 1) commit(L::bQEmpty + i);
           }
-        ptx::mma_commit(bar(L::bKVEmpty + k_slot));
+        commit(L::bKVEmpty + k_slot);
 
         for (int j = 0; ok && j < w.n_max; ++j) {
           uint32_t v_slot = 0, kn_slot = 0;
@@ -438,8 +449,8 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
               FATTN_TRACE_EV(k, j, 25 + 2 * i);
               ptx::tc_fence_after();
               issue_pv(i, v_slot, j > 0);
-              ptx::mma_commit(bar(L::bPVDone + i));
-              if (i == last_pv) ptx::mma_commit(bar(L::bKVEmpty + v_slot));
+              commit(L::bPVDone + i);
+              if (i == last_pv) commit(L::bKVEmpty + v_slot);
             }
             if (j + 1 < n[i]) {
               if (!have_kn) {
@@ -451,17 +462,17 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
               }
               FATTN_TRACE_EV(k, j, 26 + 2 * i);
               issue_s(i, kn_slot);
-              ptx::mma_commit(bar(L::bSFull + i));
-              if (j + 2 == n[i]) ptx::mma_commit(bar(L::bQEmpty + i));
+              commit(L::bSFull + i);
+              if (j + 2 == n[i]) commit(L::bQEmpty + i);
             }
           }
-          if (have_kn) ptx::mma_commit(bar(L::bKVEmpty + kn_slot));
+          if (have_kn) commit(L::bKVEmpty + kn_slot);
         }
         for (int i = 0; i < QT; ++i)
           if (n[i] > 0) ++used[i];
       }
-      // Drain: every MMA this thread issued completes before TMEM is freed.
-      ptx::mma_commit(bar(L::bDrain));
+      // Drain: every MMA this warp issued completes before TMEM is freed.
+      commit(L::bDrain);
       ptx::mbar_wait(bar(L::bDrain), 0, abort_flag, tmo);
     }
   } else if (warp < W::kCorrection0) {
