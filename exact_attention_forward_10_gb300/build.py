@@ -5,6 +5,9 @@ library) and are linked into one shared library with the CUDA runtime linked
 statically, so the library loads on machines without a GPU driver.
 
     python -m exact_attention_forward_10_gb300.build [--verbose]
+
+Extra nvcc flags (for experiments, e.g. -DFATTN_WAIT_SPIN=1) may be given in
+the FATTN_NVCC_FLAGS environment variable; they force a rebuild.
 """
 from __future__ import annotations
 
@@ -49,6 +52,7 @@ def _compile(src: str, verbose: bool) -> str:
     obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17",
            "-Xcompiler", "-fPIC,-fvisibility=hidden", "-I", INCLUDE,
+           *os.environ.get("FATTN_NVCC_FLAGS", "").split(),
            "-c", os.path.join(CSRC, src), "-o", obj]
     if verbose:
         cmd[1:1] = ["-Xptxas", "-v"]
@@ -62,7 +66,7 @@ def _compile(src: str, verbose: bool) -> str:
 
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile every translation unit and link ``libfattn.so``."""
-    if not force and not verbose and up_to_date():
+    if not force and not verbose and up_to_date() and not os.environ.get("FATTN_NVCC_FLAGS"):
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
     with concurrent.futures.ThreadPoolExecutor(len(SOURCES)) as ex:

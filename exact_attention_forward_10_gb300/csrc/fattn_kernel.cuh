@@ -35,6 +35,7 @@
 #include <cuda_fp16.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "fattn_status.h"
 #include "ptx.cuh"
@@ -53,6 +54,9 @@ constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kSwizzleChunkCols = 64;           // 128 bytes of 16-bit values
 constexpr int kChunkBytes = kBM * 128;          // one [128 rows, 64 cols] chunk
 constexpr uint32_t kTmemCols = 512;
+// A row's reference maximum moves only when the new maximum exceeds it by
+// more than this (log2 units), so every p = exp2(s*c - m) stays <= 2^8.
+constexpr float kRescaleLog2 = 8.0f;
 
 struct FwdParams {
   void* o;            // [BH, S, D] 16-bit
@@ -82,15 +86,13 @@ struct FwdLayout {
   static constexpr int bSFull = bKVEmpty + NS;
   static constexpr int bPFull = bSFull + QT;
   static constexpr int bStats = bPFull + QT;
-  static constexpr int bOReady = bStats + QT;
-  static constexpr int bPVDone = bOReady + QT;
+  static constexpr int bPVDone = bStats + QT;
   static constexpr int bOEmpty = bPVDone + QT;
   static constexpr int bDrain = bOEmpty + QT;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kMisc = kBars + kNumBars * 8;   // tmem base, abort flag
-  static constexpr int kAlpha = kMisc + 16;            // float [QT][128]
-  static constexpr int kRowL = kAlpha + QT * kBM * 4;  // float [QT][128]
-  static constexpr int kRowM = kRowL + QT * kBM * 4;   // float [QT][128]
+  static constexpr int kRowL = kMisc + 16;             // float [QT][128]
+  static constexpr int kRowM = kRowL + QT * kBM * 4;   // float [QT][128]: LSE
   static constexpr int kEnd = kRowM + QT * kBM * 4;
   static constexpr int kSmemBytes = kEnd + 1024;       // + alignment slack
   // TMEM columns
@@ -110,9 +112,9 @@ struct FwdWarps {
   // Registers per thread after the per-warpgroup split (QT == 2 only): the
   // softmax warpgroups hold a 128-float score row; the shares add up to the
   // 128 per thread the 512-thread block is launched with.
-  static constexpr int kRegSoftmax = 160;
-  static constexpr int kRegCorrection = 96;
-  static constexpr int kRegOther = 96;
+  static constexpr int kRegSoftmax = 184;
+  static constexpr int kRegCorrection = 72;
+  static constexpr int kRegOther = 72;
   static_assert(QT != 2 || 2 * kRegSoftmax + kRegCorrection + kRegOther ==
                                4 * (65536 / kThreads),
                 "register split must equal the launch allocation");
@@ -202,6 +204,25 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// The two fp32 values of a packed 16-bit pair (low half first).
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+  if constexpr (BF16) {
+    return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+  } else {
+    __half2 h = *reinterpret_cast<__half2*>(&v);
+    return __half22float2(h);
+  }
+}
+
+// Row sums of one exponent pass: of the fp32 p (for the log-sum-exp) and of
+// the 16-bit P the PV MMA actually multiplies (for normalising O, so the
+// weights applied to V sum to one exactly as rounded).
+struct RowSums {
+  float exact;
+  float rounded;
+};
+
 template <int D, int QT, int NS, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
     fattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -220,7 +241,6 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
   const uint32_t bars = base + L::kBars;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
-  float* const sAlpha = reinterpret_cast<float*>(smem + L::kAlpha);
   float* const sRowL = reinterpret_cast<float*>(smem + L::kRowL);
   float* const sRowM = reinterpret_cast<float*>(smem + L::kRowM);
 
@@ -237,7 +257,6 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       ptx::mbar_init(bar(L::bSFull + i), 1);
       ptx::mbar_init(bar(L::bPFull + i), kBM);
       ptx::mbar_init(bar(L::bStats + i), kBM);
-      ptx::mbar_init(bar(L::bOReady + i), kBM);
       ptx::mbar_init(bar(L::bPVDone + i), 1);
       ptx::mbar_init(bar(L::bOEmpty + i), kBM);
     }
@@ -323,10 +342,10 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       // Never leave with copies in flight into this CTA's shared memory.
       for (int s = 0; s < NS; ++s)
         if (kv_filled & (1u << s))
-          ptx::mbar_wait(bar(L::bKVFull + s), (kv_fill_ph >> s) & 1u, abort_flag, tmo);
+          ptx::mbar_wait_drain(bar(L::bKVFull + s), (kv_fill_ph >> s) & 1u, tmo);
       for (int i = 0; i < QT; ++i)
         if (q_uses[i] > 0)
-          ptx::mbar_wait(bar(L::bQFull + i), (q_uses[i] - 1) & 1, abort_flag, tmo);
+          ptx::mbar_wait_drain(bar(L::bQFull + i), (q_uses[i] - 1) & 1, tmo);
     }
   } else if (warp == W::kMma) {
     // ------------------------------------------------------------- MMA warp
@@ -339,8 +358,8 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       constexpr uint32_t kIdS = ptx::idesc_f16(BF16 ? 1 : 0, kBM, kBN, 0, 0);
       constexpr uint32_t kIdPV = ptx::idesc_f16(BF16 ? 1 : 0, kBM, D, 0, 1);
       uint32_t kv_idx = 0, kv_ph = 0;
-      int q_uses[QT], p_cnt[QT], or_cnt[QT], oe_cnt[QT], used[QT];
-      for (int i = 0; i < QT; ++i) q_uses[i] = p_cnt[i] = or_cnt[i] = oe_cnt[i] = used[i] = 0;
+      int q_uses[QT], p_cnt[QT], oe_cnt[QT], used[QT];
+      for (int i = 0; i < QT; ++i) q_uses[i] = p_cnt[i] = oe_cnt[i] = used[i] = 0;
       bool ok = true;
 
       auto wait_or_fail = [&](int slot, uint32_t parity) -> bool {
@@ -436,16 +455,16 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
             if (j < n[i]) last_pv = i;
           for (int i = 0; ok && i < QT; ++i) {
             if (j < n[i]) {
+              if (i == QT - 1) FATTN_TRACE_EV(k, j, 29);
               ok = wait_or_fail(L::bPFull + i, p_cnt[i] & 1);
               ++p_cnt[i];
-              if (ok && j > 0) {
-                ok = wait_or_fail(L::bOReady + i, or_cnt[i] & 1);
-                ++or_cnt[i];
-              } else if (ok && used[i] > 0) {
+              if (i == QT - 1) FATTN_TRACE_EV(k, j, 30);
+              if (ok && j == 0 && used[i] > 0) {
                 ok = wait_or_fail(L::bOEmpty + i, oe_cnt[i] & 1);
                 ++oe_cnt[i];
               }
               if (!ok) break;
+              if (i == QT - 1) FATTN_TRACE_EV(k, j, 31);
               FATTN_TRACE_EV(k, j, 25 + 2 * i);
               ptx::tc_fence_after();
               issue_pv(i, v_slot, j > 0);
@@ -473,7 +492,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       }
       // Drain: every MMA this warp issued completes before TMEM is freed.
       commit(L::bDrain);
-      ptx::mbar_wait(bar(L::bDrain), 0, abort_flag, tmo);
+      ptx::mbar_wait_drain(bar(L::bDrain), 0, tmo);
     }
   } else if (warp < W::kCorrection0) {
     // ---------------------------------------------------- softmax warpgroups
@@ -484,6 +503,45 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
     const uint32_t s_addr = tmem + ((uint32_t)(quarter * 32) << 16) + L::colS(i);
     const float c = p.scale_log2;
     int sf_cnt = 0;
+    int units_done = 0;  // units of this tile whose row statistics were published
+    // p = exp2(s*c - mref) for the row, with the scale folded into one packed
+    // FFMA per pair; 16-bit P goes to TMEM over the S columns (the whole row
+    // is in registers); both row sums run in packed partial sums; with
+    // TRACK the row maximum of s is taken on the side.
+    auto exp_pass = [&](const float (&s)[kBN], float mref, uint32_t addr, auto track_c,
+                        float& tmax) -> RowSums {
+      constexpr bool kTrack = decltype(track_c)::value;
+      const float2 c2 = make_float2(c, c);
+      const float2 neg2 = make_float2(-mref, -mref);
+      float2 sum2[4], sumr2[4];
+      float acc[8];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) sum2[a] = sumr2[a] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int a = 0; a < 8; ++a) acc[a] = -INFINITY;
+#pragma unroll
+      for (int ch = 0; ch < kBN / 32; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float s0 = s[ch * 32 + 2 * e], s1 = s[ch * 32 + 2 * e + 1];
+          if (kTrack) acc[e & 7] = fmax3(acc[e & 7], s0, s1);
+          const float2 x = __ffma2_rn(make_float2(s0, s1), c2, neg2);
+          const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+          sum2[e & 3] = __fadd2_rn(sum2[e & 3], pp);
+          pk[e] = pack2<BF16>(pp.x, pp.y);
+          sumr2[e & 3] = __fadd2_rn(sumr2[e & 3], unpack2<BF16>(pk[e]));
+        }
+        ptx::tmem_st16(addr + ch * 16, pk);
+      }
+      if (kTrack)
+        tmax = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
+                     fmaxf(acc[6], acc[7]));
+      const float2 s4 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
+      const float2 r4 =
+          __fadd2_rn(__fadd2_rn(sumr2[0], sumr2[1]), __fadd2_rn(sumr2[2], sumr2[3]));
+      return RowSums{s4.x + s4.y, r4.x + r4.y};
+    };
     for (int k = 0; k * (int)gridDim.x < p.total_units; ++k) {
       const int t = unit_of_round(k);
       if (t >= p.total_units) continue;
@@ -491,8 +549,12 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
       const int nk = n[i];
       if (nk == 0) continue;
-      float m = -INFINITY;  // running max of scaled scores (log2 domain)
-      float l = 0.f;        // running sum of exp2(s*c - m)
+      // m: the row's reference maximum of scaled scores (log2 domain), moved
+      // only when a new maximum exceeds it by more than kRescaleLog2; l: the
+      // running sum of exp2(s*c - m) with that same reference.
+      float m = -INFINITY;
+      float l = 0.f;   // sum of fp32 p (log-sum-exp)
+      float lr = 0.f;  // sum of the rounded 16-bit P (normaliser of O)
       bool ok = true;
       for (int j = 0; j < nk; ++j) {
         FATTN_TRACE_EV(k, j, 8 * i + 0);
@@ -526,59 +588,80 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < kBN; ++e) s[e] = e < limit ? s[e] : -INFINITY;
         }
-        // row max: 8 independent chains of 3-input maxima, then combined
-        float acc[8];
+        // Reference maximum m (log2 domain).  The first tile of a row has
+        // none yet: take its maximum first.  Later tiles exponentiate against
+        // the current reference at once and track their maximum on the side;
+        // the rare tile whose maximum passes the reference by more than
+        // kRescaleLog2 is redone against the new maximum (warp-uniformly,
+        // since P goes back to TMEM with warp-wide stores).  O, l and the
+        // exponent share the reference, so any choice is exact; p <= 2^8.
+        float m_use = m;
+        if (j == 0) {
+          float acc[8];
 #pragma unroll
-        for (int a = 0; a < 8; ++a) acc[a] = fmax3(s[2 * a], s[2 * a + 1], -INFINITY);
+          for (int a = 0; a < 8; ++a) acc[a] = fmax3(s[2 * a], s[2 * a + 1], -INFINITY);
 #pragma unroll
-        for (int e = 16; e < kBN; e += 16) {
+          for (int e = 16; e < kBN; e += 16) {
 #pragma unroll
-          for (int a = 0; a < 8; ++a) acc[a] = fmax3(acc[a], s[e + 2 * a], s[e + 2 * a + 1]);
-        }
-        const float mx = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
-                               fmaxf(acc[6], acc[7]));
-        const float m_new = fmaxf(m, mx * c);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = ex2(m - m_use);
-        FATTN_TRACE_EV(k, j, 8 * i + 3);
-        if (j > 0) {
-          sAlpha[i * kBM + r] = alpha;
-          ptx::mbar_arrive(bar(L::bStats + i));
-        }
-        // p = exp2(s*c - m) with the scale folded into one packed FFMA per
-        // pair; the row sum runs in four packed partial sums
-        const float2 c2 = make_float2(c, c);
-        const float2 neg2 = make_float2(-m_use, -m_use);
-        float2 sum2[4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) sum2[a] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int ch = 0; ch < kBN / 32; ++ch) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float2 x = __ffma2_rn(make_float2(s[ch * 32 + 2 * e], s[ch * 32 + 2 * e + 1]),
-                                        c2, neg2);
-            const float2 pp = make_float2(ex2(x.x), ex2(x.y));
-            sum2[e & 3] = __fadd2_rn(sum2[e & 3], pp);
-            pk[e] = pack2<BF16>(pp.x, pp.y);
+            for (int a = 0; a < 8; ++a) acc[a] = fmax3(acc[a], s[e + 2 * a], s[e + 2 * a + 1]);
           }
-          ptx::tmem_st16(s_addr + ch * 16, pk);
+          m_use = c * fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
+                            fmaxf(acc[6], acc[7]));
+          if (m_use == -INFINITY) m_use = 0.f;  // no allowed key in this row
         }
-        const float2 s01 = __fadd2_rn(sum2[0], sum2[1]);
-        const float2 s23 = __fadd2_rn(sum2[2], sum2[3]);
-        const float2 s4 = __fadd2_rn(s01, s23);
-        const float sum = s4.x + s4.y;
+        FATTN_TRACE_EV(k, j, 8 * i + 3);
+        float tmax = -INFINITY;
+        RowSums sum = exp_pass(s, m_use, s_addr, std::true_type{}, tmax);
+        float alpha = 1.0f;
+        if (j > 0) {
+          const float mxc = tmax * c;
+          const bool move = mxc > m + kRescaleLog2;
+          if (__any_sync(0xffffffffu, move)) {
+            if (move) {
+              m_use = mxc;
+              alpha = ex2(m - m_use);
+            }
+            sum = exp_pass(s, m_use, s_addr, std::false_type{}, tmax);
+          }
+        }
+        // A row that moved its reference scales its O by exp2(m_old - m_new).
+        // This warp owns these O rows (its TMEM lane quarter) and may touch
+        // them now: S_i(j) was issued after PV_i(j-1), so PV_i(j-1) has
+        // landed, and no MMA writes O_i until this warp reports P ready.
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          const uint32_t o_addr = tmem + ((uint32_t)(quarter * 32) << 16) + L::colO(i);
+#pragma unroll
+          for (int ch = 0; ch < D / 32; ++ch) {
+            uint32_t u[32];
+            ptx::tmem_ld32(o_addr + ch * 32, u);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+            ptx::tmem_st32(o_addr + ch * 32, u);
+          }
+        }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::bPFull + i));
         FATTN_TRACE_EV(k, j, 8 * i + 4);
-        l = alpha * l + sum;
+        l = alpha * l + sum.exact;
+        lr = alpha * lr + sum.rounded;
         m = m_use;
       }
       if (!ok) break;
-      sRowL[i * kBM + r] = l;
-      sRowM[i * kBM + r] = m;
+      // The previous unit's epilogue must have read its statistics before
+      // they are overwritten; it releases O_i (o_empty) after reading them.
+      if (units_done > 0) {
+        ok = ptx::mbar_wait(bar(L::bOEmpty + i), (units_done - 1) & 1, abort_flag, tmo);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          if (lane == 0) raise_error(p, abort_flag, kErrPipelineTimeout, kRoleSoftmax, L::bOEmpty + i);
+          break;
+        }
+      }
+      ++units_done;
+      sRowL[i * kBM + r] = lr;
+      sRowM[i * kBM + r] = (m + log2f(l)) * 0.69314718055994531f;  // natural-log LSE
       ptx::mbar_arrive(bar(L::bStats + i));
     }
   } else if (warp < W::kMma) {
@@ -587,8 +670,11 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
     const int quarter = warp % 4;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    int st_cnt[QT], pd_cnt[QT];
-    for (int i = 0; i < QT; ++i) st_cnt[i] = pd_cnt[i] = 0;
+    // st_cnt: units whose final row statistics were read; pv_base: PV MMAs
+    // of earlier units, so the phase of "last PV_i of this unit done" is
+    // known without waiting on every PV.
+    int st_cnt[QT], pv_base[QT];
+    for (int i = 0; i < QT; ++i) st_cnt[i] = pv_base[i] = 0;
     bool ok = true;
     auto wait_all = [&](int slot, uint32_t parity) -> bool {
       bool w_ok = ptx::mbar_wait(bar(slot), parity, abort_flag, tmo);
@@ -602,46 +688,15 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       if (t >= p.total_units) continue;
       int n[QT];
       const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
-      for (int j = 1; ok && j < w.n_max; ++j) {
-        for (int i = 0; i < QT; ++i) {
-          if (j >= n[i]) continue;
-          FATTN_TRACE_EV(k, j, 16 + 4 * i + 0);
-          if (!wait_all(L::bStats + i, st_cnt[i] & 1)) { ok = false; break; }
-          ++st_cnt[i];
-          FATTN_TRACE_EV(k, j, 16 + 4 * i + 1);
-          const float a = sAlpha[i * kBM + r];
-          if (!wait_all(L::bPVDone + i, pd_cnt[i] & 1)) { ok = false; break; }
-          ++pd_cnt[i];
-          FATTN_TRACE_EV(k, j, 16 + 4 * i + 2);
-          if (__any_sync(0xffffffffu, a != 1.f)) {
-            ptx::tc_fence_after();
-            const uint32_t o_addr = tmem + lane_off + L::colO(i);
-#pragma unroll
-            for (int ch = 0; ch < D / 32; ++ch) {
-              uint32_t u[32];
-              ptx::tmem_ld32(o_addr + ch * 32, u);
-              ptx::tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * a);
-              ptx::tmem_st32(o_addr + ch * 32, u);
-            }
-            ptx::tmem_wait_st();
-          }
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(bar(L::bOReady + i));
-          FATTN_TRACE_EV(k, j, 16 + 4 * i + 3);
-        }
-      }
-      if (!ok) break;
       // epilogue: O = acc / l (one reciprocal per row), LSE = ln2 (m + log2 l)
       for (int i = 0; i < QT; ++i) {
         if (n[i] == 0) continue;
         if (!wait_all(L::bStats + i, st_cnt[i] & 1)) { ok = false; break; }
         ++st_cnt[i];
-        const float l = sRowL[i * kBM + r];
-        const float m = sRowM[i * kBM + r];
-        if (!wait_all(L::bPVDone + i, pd_cnt[i] & 1)) { ok = false; break; }
-        ++pd_cnt[i];
+        const float l = sRowL[i * kBM + r];    // sum of the rounded P
+        const float lse = sRowM[i * kBM + r];  // log-sum-exp of the row
+        if (!wait_all(L::bPVDone + i, (uint32_t)(pv_base[i] + n[i] - 1) & 1u)) { ok = false; break; }
+        pv_base[i] += n[i];
         ptx::tc_fence_after();
         const float inv_l = 1.0f / l;
         const int row = w.q_row0 + kBM * i + r;
@@ -666,7 +721,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
               orow[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
           }
         }
-        if (valid) p.lse[grow] = (m + log2f(l)) * 0.69314718055994531f;
+        if (valid) p.lse[grow] = lse;
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::bOEmpty + i));
       }

@@ -88,20 +88,55 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// True once the phase with the given parity has completed; never suspends.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// FATTN_WAIT_SPIN=1 polls with test_wait (no suspension) instead of try_wait.
+#ifndef FATTN_WAIT_SPIN
+#define FATTN_WAIT_SPIN 0
+#endif
+
 // Bounded wait: polls until the phase completes, the CTA-wide abort flag is
 // raised, or ``timeout_ns`` of wall time passes.  Returns false on the last
 // two.  No wait in this library is unbounded.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           const volatile int* abort_flag,
                                           uint64_t timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&]() {
+    return FATTN_WAIT_SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll()) return true;
     if ((it & 31u) == 0u) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > timeout_ns) return false;
     }
+  }
+}
+
+// Bounded wait for work this CTA itself has in flight (its own MMAs or TMA
+// copies) before it frees TMEM or exits: only the time limit ends it early,
+// never the abort flag, so an unwinding CTA does not leave asynchronous
+// writes into memory it is about to release.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
+                                                uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0u && globaltimer_ns() - t0 > timeout_ns) return false;
   }
 }
 

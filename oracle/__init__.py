@@ -134,7 +134,7 @@ def attn_fwd_numpy(q, k, v, causal: bool, scale: float, want_p: bool = False):
 
 
 def attn_fwd_online(q, k, v, causal: bool, scale: float, block_m: int = 128,
-                    block_n: int = 128):
+                    block_n: int = 128, lazy_threshold: float = 0.0):
     """Online-softmax recurrence in fp64, tile by tile.
 
     For each query tile: running max ``m`` (start -inf), running sum ``l``
@@ -145,6 +145,10 @@ def attn_fwd_online(q, k, v, causal: bool, scale: float, block_m: int = 128,
     ``p = exp(s - m_new)``, ``l = alpha * l + rowsum(p)``,
     ``acc = alpha * acc + p V``, ``m = m_new``.  After the last key tile
     ``O = acc / l`` (one division) and ``LSE = m + ln l``.
+
+    ``lazy_threshold > 0`` keeps the reference maximum until a tile's maximum
+    exceeds it by more than that amount (natural-log units); the algebra is
+    unchanged because ``acc``, ``l`` and the exponent share the reference.
     """
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, H, S, D = q.shape
@@ -167,6 +171,9 @@ def attn_fwd_online(q, k, v, causal: bool, scale: float, block_m: int = 128,
                     if causal:
                         s = np.where(rows[:, None] >= cols[None, :], s, -np.inf)
                     m_new = np.maximum(m, s.max(axis=1))
+                    if lazy_threshold > 0:
+                        m_new = np.where(s.max(axis=1) > m + lazy_threshold,
+                                         m_new, m)
                     alpha = np.exp(m - m_new)
                     p = np.exp(s - m_new[:, None])
                     l = alpha * l + p.sum(axis=1)

@@ -320,6 +320,19 @@ def test_online_recurrence_equals_definition(bm, bn):
         np.testing.assert_allclose(l1, l2, atol=1e-13)
 
 
+@pytest.mark.parametrize("thr", [0.5, 8.0 * math.log(2.0)])
+def test_lazy_reference_max_equals_definition(thr):
+    """Keeping a stale reference maximum (moved only when a tile's maximum
+    exceeds it by more than a threshold) changes nothing: O, l and the
+    exponent share the reference.  Large scores make the maximum move."""
+    q, k, v = 4 * rnd(1, 2, 300, 16), 4 * rnd(1, 2, 300, 16), rnd(1, 2, 300, 16)
+    for causal in (False, True):
+        o1, l1 = oracle.attn_fwd_online(q, k, v, causal, 0.3, 32, 32, thr)
+        o2, l2 = oracle.attn_fwd(q, k, v, causal, 0.3)
+        np.testing.assert_allclose(o1, o2, atol=1e-12)
+        np.testing.assert_allclose(l1, l2, atol=1e-12)
+
+
 def test_row_subset_equals_full():
     q, k, v = rnd(2, 2, 50, 8), rnd(2, 2, 50, 8), rnd(2, 2, 50, 8)
     rows = np.array([0, 49, 50, 77, 199, 3])
