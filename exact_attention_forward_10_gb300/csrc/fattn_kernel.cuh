@@ -112,9 +112,9 @@ struct FwdWarps {
   // Registers per thread after the per-warpgroup split (QT == 2 only): the
   // softmax warpgroups hold a 128-float score row; the shares add up to the
   // 128 per thread the 512-thread block is launched with.
-  static constexpr int kRegSoftmax = 184;
-  static constexpr int kRegCorrection = 72;
-  static constexpr int kRegOther = 72;
+  static constexpr int kRegSoftmax = 176;
+  static constexpr int kRegCorrection = 80;
+  static constexpr int kRegOther = 80;
   static_assert(QT != 2 || 2 * kRegSoftmax + kRegCorrection + kRegOther ==
                                4 * (65536 / kThreads),
                 "register split must equal the launch allocation");
@@ -214,14 +214,6 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
     return __half22float2(h);
   }
 }
-
-// Row sums of one exponent pass: of the fp32 p (for the log-sum-exp) and of
-// the 16-bit P the PV MMA actually multiplies (for normalising O, so the
-// weights applied to V sum to one exactly as rounded).
-struct RowSums {
-  float exact;
-  float rounded;
-};
 
 template <int D, int QT, int NS, bool CAUSAL, bool BF16>
 __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
@@ -506,17 +498,17 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
     int units_done = 0;  // units of this tile whose row statistics were published
     // p = exp2(s*c - mref) for the row, with the scale folded into one packed
     // FFMA per pair; 16-bit P goes to TMEM over the S columns (the whole row
-    // is in registers); both row sums run in packed partial sums; with
-    // TRACK the row maximum of s is taken on the side.
+    // is in registers), the row sum runs in four packed partial sums, and
+    // with TRACK the row maximum of s is taken on the side.
     auto exp_pass = [&](const float (&s)[kBN], float mref, uint32_t addr, auto track_c,
-                        float& tmax) -> RowSums {
+                        float& tmax) -> float {
       constexpr bool kTrack = decltype(track_c)::value;
       const float2 c2 = make_float2(c, c);
       const float2 neg2 = make_float2(-mref, -mref);
-      float2 sum2[4], sumr2[4];
+      float2 sum2[4];
       float acc[8];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) sum2[a] = sumr2[a] = make_float2(0.f, 0.f);
+      for (int a = 0; a < 4; ++a) sum2[a] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int a = 0; a < 8; ++a) acc[a] = -INFINITY;
 #pragma unroll
@@ -530,7 +522,6 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           const float2 pp = make_float2(ex2(x.x), ex2(x.y));
           sum2[e & 3] = __fadd2_rn(sum2[e & 3], pp);
           pk[e] = pack2<BF16>(pp.x, pp.y);
-          sumr2[e & 3] = __fadd2_rn(sumr2[e & 3], unpack2<BF16>(pk[e]));
         }
         ptx::tmem_st16(addr + ch * 16, pk);
       }
@@ -538,9 +529,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         tmax = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
                      fmaxf(acc[6], acc[7]));
       const float2 s4 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
-      const float2 r4 =
-          __fadd2_rn(__fadd2_rn(sumr2[0], sumr2[1]), __fadd2_rn(sumr2[2], sumr2[3]));
-      return RowSums{s4.x + s4.y, r4.x + r4.y};
+      return s4.x + s4.y;
     };
     for (int k = 0; k * (int)gridDim.x < p.total_units; ++k) {
       const int t = unit_of_round(k);
@@ -554,7 +543,8 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       // running sum of exp2(s*c - m) with that same reference.
       float m = -INFINITY;
       float l = 0.f;   // sum of fp32 p (log-sum-exp)
-      float lr = 0.f;  // sum of the rounded 16-bit P (normaliser of O)
+      float lr = 0.f;  // the same with each tile's largest p rounded as the
+                       // MMA multiplies it (normaliser of O)
       bool ok = true;
       for (int j = 0; j < nk; ++j) {
         FATTN_TRACE_EV(k, j, 8 * i + 0);
@@ -611,7 +601,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         }
         FATTN_TRACE_EV(k, j, 8 * i + 3);
         float tmax = -INFINITY;
-        RowSums sum = exp_pass(s, m_use, s_addr, std::true_type{}, tmax);
+        float sum = exp_pass(s, m_use, s_addr, std::true_type{}, tmax);
         float alpha = 1.0f;
         if (j > 0) {
           const float mxc = tmax * c;
@@ -644,8 +634,15 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::bPFull + i));
         FATTN_TRACE_EV(k, j, 8 * i + 4);
-        l = alpha * l + sum.exact;
-        lr = alpha * lr + sum.rounded;
+        // The tile's largest weight, as the MMA sees it (rounded to 16 bits):
+        // normalising O by the fp32 sum with that one term replaced keeps a
+        // peaked row's dominant weight exact, as p = 1 would be under an
+        // exact running maximum.  (fmaf gives the same value as a lane of
+        // the packed FFMA above.)
+        const float pt = ex2(fmaf(tmax, c, -m_use));
+        const float pt16 = unpack2<BF16>(pack2<BF16>(pt, 0.f)).x;
+        l = alpha * l + sum;
+        lr = alpha * lr + (sum + (pt16 - pt));
         m = m_use;
       }
       if (!ok) break;
@@ -693,7 +690,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         if (n[i] == 0) continue;
         if (!wait_all(L::bStats + i, st_cnt[i] & 1)) { ok = false; break; }
         ++st_cnt[i];
-        const float l = sRowL[i * kBM + r];    // sum of the rounded P
+        const float l = sRowL[i * kBM + r];    // normaliser of O
         const float lse = sRowM[i * kBM + r];  // log-sum-exp of the row
         if (!wait_all(L::bPVDone + i, (uint32_t)(pv_base[i] + n[i] - 1) & 1u)) { ok = false; break; }
         pv_base[i] += n[i];
