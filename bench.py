@@ -406,6 +406,59 @@ def cpu_baseline(x, w) -> dict:
                       f"({dt:.1f} s); metric FLOPs of those rows / wall time"}
 
 
+def run_sweep(args):
+    """Attention TFLOPS over the sweep shapes (B2 H16; S 512 .. 16384 and
+    4097; D 64, 128; fp16, bf16; both masks): one JSON line per point.
+    Timing inputs come from torch's generator on the device (the same i.i.d.
+    N(0,1) distribution; parity over these shapes is the tests' job)."""
+    import torch
+
+    import exact_attention_forward_10_gb300 as fattn
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(dev)
+    for w in attn_inputs.sweep_workloads():
+        tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+        code = fattn.FATTN_BF16 if w.dtype == "bf16" else fattn.FATTN_FP16
+        g = torch.Generator(device=dev)
+        g.manual_seed(w.seed)
+        q, k, v = (torch.randn(w.B, w.H, w.S, w.D, device=dev, dtype=torch.float32,
+                               generator=g).to(tdt) for _ in range(3))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+        for causal in w.causal:
+            def launch():
+                rc = fattn.fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr(), w.B, w.H, w.S, w.D, causal, w.scale,
+                                     code, stream.cuda_stream)
+                if rc != 0:
+                    raise fattn.FattnError(rc)
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    launch()
+            torch.cuda.synchronize(dev)
+            times = []
+            for _ in range(max(20, args.steps)):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    a.record(stream)
+                    launch()
+                    b.record(stream)
+                times.append((a, b))
+            torch.cuda.synchronize(dev)
+            ms = statistics.median(x.elapsed_time(y) for x, y in times)
+            rc, where = fattn.fattn_last_error(stream.cuda_stream)
+            if rc != 0:
+                raise RuntimeError(f"kernel status {rc} at {where}")
+            tf = metric_flops(w.B, w.H, w.S, w.D, causal) / (ms * 1e-3) / 1e12
+            print(json.dumps({"S": w.S, "D": w.D, "dtype": w.dtype, "causal": causal,
+                              "ms_median": ms, "tflops": tf,
+                              "frac_of_measured_peak": tf / peaks["burst"]}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -413,9 +466,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="fattn", choices=["fattn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="TFLOPS over the sweep shapes, one JSON line each")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_fattn(args)
