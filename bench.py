@@ -52,8 +52,9 @@ def workload_config(w, extra=None) -> dict:
     c = {"workload": f"B{w.B} H{w.H} S{w.S} D{w.D} {w.dtype}, non-causal + "
                      f"causal, Q/K/V iid N(0,1) seed {w.seed}, scale 1/sqrt(D)",
          "B": w.B, "H": w.H, "S": w.S, "D": w.D, "masks": "non-causal+causal",
-         "l2": "inputs larger than L2 (Q,K,V 192 MiB + O 64 MiB per launch); "
-               "no flush"}
+         "l2": (f"inputs larger than L2 (Q,K,V {3 * 2 * w.B * w.H * w.S * w.D / 2**20:.0f} MiB); "
+                "no flush") if 3 * 2 * w.B * w.H * w.S * w.D > 160e6 else
+               "inputs smaller than L2; no flush between steps"}
     if extra:
         c.update(extra)
     return c
@@ -468,7 +469,18 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="TFLOPS over the sweep shapes, one JSON line each")
+    ap.add_argument("--shape", default=None,
+                    help="S,D,dtype of a sweep shape (B2 H16) to use as the step "
+                         "workload instead of B2 H16 S8192 D128 bf16, e.g. 8192,64,bf16")
     args = ap.parse_args()
+    if args.shape:
+        S, D, dt = args.shape.split(",")
+        picks = [w for w in attn_inputs.sweep_workloads()
+                 if (w.S, w.D, w.dtype) == (int(S), int(D), dt)]
+        if not picks:
+            ap.error(f"no sweep shape {args.shape}")
+        global WORKLOAD
+        WORKLOAD = picks[0]
     if args.warmup < 3:
         args.warmup = 3
     if args.sweep:

@@ -44,11 +44,20 @@
 // event of the pipeline when an instrumented build defines it; the product
 // build compiles it to nothing.
 #ifndef FATTN_TRACE_EV
+#define FATTN_TRACE_INIT ((void)0)
 #define FATTN_TRACE_EV(round, kv_tile, event) ((void)0)
+#endif
+
+// Roles whose barrier waits spin instead of suspending (bit 0: load warp,
+// bit 1: MMA warp); a build-time choice.
+#ifndef FATTN_SPIN_ROLES
+#define FATTN_SPIN_ROLES 0
 #endif
 
 namespace fattn {
 
+constexpr bool kSpinLoad = (FATTN_SPIN_ROLES & 1) != 0;
+constexpr bool kSpinMma = (FATTN_SPIN_ROLES & 2) != 0;
 constexpr int kBM = 128;  // query rows per tile (one TMEM lane each)
 constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kSwizzleChunkCols = 64;           // 128 bytes of 16-bit values
@@ -85,7 +94,8 @@ struct FwdLayout {
   static constexpr int bKVEmpty = bKVFull + NS;
   static constexpr int bSFull = bKVEmpty + NS;
   static constexpr int bPFull = bSFull + QT;
-  static constexpr int bStats = bPFull + QT;
+  static constexpr int bSFree = bPFull + QT;
+  static constexpr int bStats = bSFree + QT;
   static constexpr int bPVDone = bStats + QT;
   static constexpr int bOEmpty = bPVDone + QT;
   static constexpr int bDrain = bOEmpty + QT;
@@ -94,11 +104,21 @@ struct FwdLayout {
   static constexpr int kRowL = kMisc + 16;             // float [QT][128]
   static constexpr int kRowM = kRowL + QT * kBM * 4;   // float [QT][128]: LSE
   static constexpr int kEnd = kRowM + QT * kBM * 4;
-  static constexpr int kSmemBytes = kEnd + 1024;       // + alignment slack
-  // TMEM columns
+  // The dynamic shared memory base must be 1024-byte aligned (128-byte
+  // swizzle atoms); the kernel checks it instead of reserving slack.
+  static constexpr int kSmemBytes = kEnd;
+  // TMEM columns.  When they fit (D = 64), P_i gets its own 64 columns, so
+  // S_i(j+1) can be computed while the softmax of tile j still runs; else P_i
+  // overwrites the first 64 columns of S_i.
+  static constexpr bool kSepP = QT * (128 + 64) + QT * D <= (int)kTmemCols;
   __host__ __device__ static constexpr uint32_t colS(int i) { return 128u * i; }
-  __host__ __device__ static constexpr uint32_t colO(int i) { return 128u * QT + D * i; }
-  static_assert(128 * QT + D * QT <= (int)kTmemCols, "TMEM budget");
+  __host__ __device__ static constexpr uint32_t colP(int i) {
+    return kSepP ? 128u * QT + 64u * i : colS(i);
+  }
+  __host__ __device__ static constexpr uint32_t colO(int i) {
+    return 128u * QT + (kSepP ? 64u * QT : 0u) + D * i;
+  }
+  static_assert(colO(QT) <= kTmemCols, "TMEM budget");
 };
 
 template <int QT>
@@ -225,9 +245,16 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
   using W = FwdWarps<QT>;
   extern __shared__ uint8_t smem_raw[];
 
-  const uint32_t raw = ptx::smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* const smem = smem_raw + (base - raw);
+  const uint32_t base = ptx::smem_u32(smem_raw);
+  if (base & 1023u) {
+    // Not 1024-byte aligned: report instead of touching shared memory.
+    if (threadIdx.x == 0 && atomicCAS(p.status, 0, kErrLaunch) == 0) {
+      p.status[1] = 0;
+      p.status[2] = (int)blockIdx.x;
+    }
+    return;
+  }
+  uint8_t* const smem = smem_raw;
   const uint32_t sQ = base + L::kQ;
   const uint32_t sKV = base + L::kKV;
   const uint32_t bars = base + L::kBars;
@@ -241,6 +268,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t tmo = p.timeout_ns;
+  FATTN_TRACE_INIT;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < QT; ++i) {
@@ -248,6 +276,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       ptx::mbar_init(bar(L::bQEmpty + i), 1);
       ptx::mbar_init(bar(L::bSFull + i), 1);
       ptx::mbar_init(bar(L::bPFull + i), kBM);
+      ptx::mbar_init(bar(L::bSFree + i), kBM);
       ptx::mbar_init(bar(L::bStats + i), kBM);
       ptx::mbar_init(bar(L::bPVDone + i), 1);
       ptx::mbar_init(bar(L::bOEmpty + i), kBM);
@@ -294,7 +323,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         for (int i = 0; ok && i < QT; ++i) {
           if (n[i] == 0) continue;
           if (q_uses[i] > 0 &&
-              !ptx::mbar_wait(bar(L::bQEmpty + i), (q_uses[i] - 1) & 1, abort_flag, tmo)) {
+              !ptx::mbar_wait<kSpinLoad>(bar(L::bQEmpty + i), (q_uses[i] - 1) & 1, abort_flag, tmo)) {
             raise_error(p, abort_flag, kErrPipelineTimeout, kRoleLoad, L::bQEmpty + i);
             ok = false;
             break;
@@ -310,7 +339,8 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         for (int j = 0; ok && j < w.n_max; ++j) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
-            if (!ptx::mbar_wait(bar(L::bKVEmpty + kv_idx), kv_ph ^ 1u, abort_flag, tmo)) {
+            if (kv == 1) FATTN_TRACE_EV(k, j, 7);
+            if (!ptx::mbar_wait<kSpinLoad>(bar(L::bKVEmpty + kv_idx), kv_ph ^ 1u, abort_flag, tmo)) {
               raise_error(p, abort_flag, kErrPipelineTimeout, kRoleLoad, L::bKVEmpty + kv_idx);
               ok = false;
               break;
@@ -322,6 +352,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
               ptx::tma_load_3d(sKV + kv_idx * L::kTileBytes + c * kChunkBytes,
                                kv == 0 ? &tm_k : &tm_v, fb, c * kSwizzleChunkCols,
                                j * kBN, w.bh);
+            FATTN_TRACE_EV(k, j, 5 + kv);
             kv_filled |= 1u << kv_idx;
             kv_fill_ph = (kv_fill_ph & ~(1u << kv_idx)) | (kv_ph << kv_idx);
             if (++kv_idx == NS) {
@@ -350,12 +381,13 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       constexpr uint32_t kIdS = ptx::idesc_f16(BF16 ? 1 : 0, kBM, kBN, 0, 0);
       constexpr uint32_t kIdPV = ptx::idesc_f16(BF16 ? 1 : 0, kBM, D, 0, 1);
       uint32_t kv_idx = 0, kv_ph = 0;
-      int q_uses[QT], p_cnt[QT], oe_cnt[QT], used[QT];
-      for (int i = 0; i < QT; ++i) q_uses[i] = p_cnt[i] = oe_cnt[i] = used[i] = 0;
+      uint32_t kv_item = 0;  // separate-P layout: ring index of the next unit's K_0
+      int q_uses[QT], p_cnt[QT], oe_cnt[QT], used[QT], s_issued[QT];
+      for (int i = 0; i < QT; ++i) q_uses[i] = p_cnt[i] = oe_cnt[i] = used[i] = s_issued[i] = 0;
       bool ok = true;
 
       auto wait_or_fail = [&](int slot, uint32_t parity) -> bool {
-        bool w_ok = ptx::mbar_wait(bar(slot), parity, abort_flag, tmo);
+        bool w_ok = ptx::mbar_wait<kSpinMma>(bar(slot), parity, abort_flag, tmo);
         w_ok = __all_sync(0xffffffffu, w_ok);
         if (!w_ok && lane == 0) raise_error(p, abort_flag, kErrPipelineTimeout, kRoleMma, slot);
         return w_ok;
@@ -401,7 +433,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       // step 16 key rows (2048 bytes) further.
       auto issue_pv = [&](int i, uint32_t v_slot, bool acc) {
         const uint32_t d = tmem + L::colO(i);
-        const uint32_t a = tmem + L::colS(i);
+        const uint32_t a = tmem + L::colP(i);
         const uint32_t vb = v_lo + v_slot * kTileLo;
         if (!ptx::elect_one()) return;
 #pragma unroll
@@ -423,61 +455,145 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
             ok = wait_or_fail(L::bQFull + i, q_uses[i] & 1);
             ++q_uses[i];
           }
-        uint32_t k_slot = 0;
-        if (ok) ok = next_kv(k_slot);
         if (!ok) break;
-        for (int i = 0; i < QT; ++i)
-          if (n[i] > 0) {
-            issue_s(i, k_slot);
+        if constexpr (L::kSepP) {
+          // Separate P: S_i(j+2) needs only that the softmax has read
+          // S_i(j+1) (s_free), so each tile's scores are two steps ahead and
+          // the two softmax warpgroups run back to back.  Per step j the
+          // order is PV_0(j), S_0(j+2), PV_1(j), S_1(j+2).  K/V items are
+          // then taken slightly out of ring order (K_{j+2} before V_{j+1}),
+          // so each is addressed by its index in the ring; the reordering
+          // window (two items) is far below the ring depth.
+          static_assert(NS >= 6, "separate-P issue order needs a deeper K/V ring");
+          const uint32_t base = kv_item;  // ring index of this unit's K_0
+          kv_item += 2u * (uint32_t)w.n_max;
+          auto wait_item = [&](uint32_t idx) -> bool {
+            const uint32_t g = base + idx;
+            if (!wait_or_fail(L::bKVFull + (int)(g % NS), (g / NS) & 1u)) return false;
+            ptx::tc_fence_after();
+            return true;
+          };
+          auto item_slot = [&](uint32_t idx) -> int { return (int)((base + idx) % NS); };
+          auto issue_s_step = [&](int i, int jj) -> bool {
+            if (s_issued[i] > 0 && !wait_or_fail(L::bSFree + i, (s_issued[i] - 1) & 1))
+              return false;
+            ++s_issued[i];
+            ptx::tc_fence_after();
+            FATTN_TRACE_EV(k, jj, 26 + 2 * i);
+            issue_s(i, (uint32_t)item_slot(2u * jj));
             commit(L::bSFull + i);
-            if (n[i] == 1) commit(L::bQEmpty + i);
+            if (jj == n[i] - 1) commit(L::bQEmpty + i);
+            return true;
+          };
+          auto last_user = [&](int jj) -> int {
+            int u = -1;
+            for (int i = 0; i < QT; ++i)
+              if (jj < n[i]) u = i;
+            return u;
+          };
+          // prologue: S_i(0) and S_i(1)
+          for (int jj = 0; ok && jj < 2 && jj < w.n_max; ++jj) {
+            ok = wait_item(2u * jj);
+            for (int i = 0; ok && i < QT; ++i)
+              if (jj < n[i]) ok = issue_s_step(i, jj);
+            if (ok) commit(L::bKVEmpty + item_slot(2u * jj));
           }
-        commit(L::bKVEmpty + k_slot);
-
-        for (int j = 0; ok && j < w.n_max; ++j) {
-          uint32_t v_slot = 0, kn_slot = 0;
-          bool have_kn = false;
-          if (!next_kv(v_slot)) {
+          for (int j = 0; ok && j < w.n_max; ++j) {
+            if (!wait_item(2u * j + 1u)) {
+              ok = false;
+              break;
+            }
+            FATTN_TRACE_EV(k, j, 24);
+            const int last_v = last_user(j);
+            const int last_k = last_user(j + 2);
+            bool have_k = false;
+            for (int i = 0; ok && i < QT; ++i) {
+              if (j < n[i]) {
+                ok = wait_or_fail(L::bPFull + i, p_cnt[i] & 1);
+                ++p_cnt[i];
+                if (ok && j == 0 && used[i] > 0) {
+                  ok = wait_or_fail(L::bOEmpty + i, oe_cnt[i] & 1);
+                  ++oe_cnt[i];
+                }
+                if (!ok) break;
+                FATTN_TRACE_EV(k, j, 25 + 2 * i);
+                ptx::tc_fence_after();
+                issue_pv(i, (uint32_t)item_slot(2u * j + 1u), j > 0);
+                commit(L::bPVDone + i);
+                if (i == last_v) commit(L::bKVEmpty + item_slot(2u * j + 1u));
+              }
+              if (j + 2 < n[i]) {
+                if (!have_k) {
+                  if (!wait_item(2u * (j + 2))) {
+                    ok = false;
+                    break;
+                  }
+                  have_k = true;
+                }
+                ok = issue_s_step(i, j + 2);
+                if (ok && i == last_k) commit(L::bKVEmpty + item_slot(2u * (j + 2)));
+              }
+            }
+          }
+        } else {
+          uint32_t k_slot = 0;
+          if (!next_kv(k_slot)) {
             ok = false;
             break;
           }
-          FATTN_TRACE_EV(k, j, 24);
-          int last_pv = -1;
           for (int i = 0; i < QT; ++i)
-            if (j < n[i]) last_pv = i;
-          for (int i = 0; ok && i < QT; ++i) {
-            if (j < n[i]) {
-              if (i == QT - 1) FATTN_TRACE_EV(k, j, 29);
-              ok = wait_or_fail(L::bPFull + i, p_cnt[i] & 1);
-              ++p_cnt[i];
-              if (i == QT - 1) FATTN_TRACE_EV(k, j, 30);
-              if (ok && j == 0 && used[i] > 0) {
-                ok = wait_or_fail(L::bOEmpty + i, oe_cnt[i] & 1);
-                ++oe_cnt[i];
-              }
-              if (!ok) break;
-              if (i == QT - 1) FATTN_TRACE_EV(k, j, 31);
-              FATTN_TRACE_EV(k, j, 25 + 2 * i);
-              ptx::tc_fence_after();
-              issue_pv(i, v_slot, j > 0);
-              commit(L::bPVDone + i);
-              if (i == last_pv) commit(L::bKVEmpty + v_slot);
-            }
-            if (j + 1 < n[i]) {
-              if (!have_kn) {
-                if (!next_kv(kn_slot)) {
-                  ok = false;
-                  break;
-                }
-                have_kn = true;
-              }
-              FATTN_TRACE_EV(k, j, 26 + 2 * i);
-              issue_s(i, kn_slot);
+            if (n[i] > 0) {
+              issue_s(i, k_slot);
               commit(L::bSFull + i);
-              if (j + 2 == n[i]) commit(L::bQEmpty + i);
+              if (n[i] == 1) commit(L::bQEmpty + i);
             }
+          commit(L::bKVEmpty + k_slot);
+
+          for (int j = 0; ok && j < w.n_max; ++j) {
+            uint32_t v_slot = 0, kn_slot = 0;
+            bool have_kn = false;
+            if (!next_kv(v_slot)) {
+              ok = false;
+              break;
+            }
+            FATTN_TRACE_EV(k, j, 24);
+            int last_pv = -1;
+            for (int i = 0; i < QT; ++i)
+              if (j < n[i]) last_pv = i;
+            for (int i = 0; ok && i < QT; ++i) {
+              if (j < n[i]) {
+                if (i == QT - 1) FATTN_TRACE_EV(k, j, 29);
+                ok = wait_or_fail(L::bPFull + i, p_cnt[i] & 1);
+                ++p_cnt[i];
+                if (i == QT - 1) FATTN_TRACE_EV(k, j, 30);
+                if (ok && j == 0 && used[i] > 0) {
+                  ok = wait_or_fail(L::bOEmpty + i, oe_cnt[i] & 1);
+                  ++oe_cnt[i];
+                }
+                if (!ok) break;
+                if (i == QT - 1) FATTN_TRACE_EV(k, j, 31);
+                FATTN_TRACE_EV(k, j, 25 + 2 * i);
+                ptx::tc_fence_after();
+                issue_pv(i, v_slot, j > 0);
+                commit(L::bPVDone + i);
+                if (i == last_pv) commit(L::bKVEmpty + v_slot);
+              }
+              if (j + 1 < n[i]) {
+                if (!have_kn) {
+                  if (!next_kv(kn_slot)) {
+                    ok = false;
+                    break;
+                  }
+                  have_kn = true;
+                }
+                FATTN_TRACE_EV(k, j, 26 + 2 * i);
+                issue_s(i, kn_slot);
+                commit(L::bSFull + i);
+                if (j + 2 == n[i]) commit(L::bQEmpty + i);
+              }
+            }
+            if (have_kn) commit(L::bKVEmpty + kn_slot);
           }
-          if (have_kn) commit(L::bKVEmpty + kn_slot);
         }
         for (int i = 0; i < QT; ++i)
           if (n[i] > 0) ++used[i];
@@ -493,9 +609,11 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
     const int quarter = warp % 4;    // TMEM lanes 32*quarter .. +31
     const int r = quarter * 32 + lane;
     const uint32_t s_addr = tmem + ((uint32_t)(quarter * 32) << 16) + L::colS(i);
+    const uint32_t p_addr = tmem + ((uint32_t)(quarter * 32) << 16) + L::colP(i);
     const float c = p.scale_log2;
     int sf_cnt = 0;
     int units_done = 0;  // units of this tile whose row statistics were published
+    int p_writes = 0;    // P_i buffer fills so far (separate-P layout)
     // p = exp2(s*c - mref) for the row, with the scale folded into one packed
     // FFMA per pair; 16-bit P goes to TMEM over the S columns (the whole row
     // is in registers), the row sum runs in four packed partial sums, and
@@ -528,6 +646,24 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       if (kTrack)
         tmax = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
                      fmaxf(acc[6], acc[7]));
+      const float2 s4 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
+      return s4.x + s4.y;
+    };
+    // The same exponent pass keeping the packed P in registers (stored once
+    // the PV that last read this P buffer has completed).
+    auto exp_pack = [&](const float (&s)[kBN], float mref, uint32_t (&pk)[kBN / 2]) -> float {
+      const float2 c2 = make_float2(c, c);
+      const float2 neg2 = make_float2(-mref, -mref);
+      float2 sum2[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) sum2[a] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int e = 0; e < kBN / 2; ++e) {
+        const float2 x = __ffma2_rn(make_float2(s[2 * e], s[2 * e + 1]), c2, neg2);
+        const float2 pp = make_float2(ex2(x.x), ex2(x.y));
+        sum2[e & 3] = __fadd2_rn(sum2[e & 3], pp);
+        pk[e] = pack2<BF16>(pp.x, pp.y);
+      }
       const float2 s4 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
       return s4.x + s4.y;
     };
@@ -566,6 +702,11 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           for (int e = 0; e < 32; ++e) s[ch * 32 + e] = __uint_as_float(u[e]);
         }
         ptx::tmem_wait_ld();
+        if constexpr (L::kSepP) {
+          // S_i is in registers: the MMA may compute S_i(j+1) into it now.
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::bSFree + i));
+        }
         FATTN_TRACE_EV(k, j, 8 * i + 2);
         // masks: causal diagonal tile keeps key <= query; keys >= S removed
         const int kv0 = j * kBN;
@@ -578,15 +719,10 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < kBN; ++e) s[e] = e < limit ? s[e] : -INFINITY;
         }
-        // Reference maximum m (log2 domain).  The first tile of a row has
-        // none yet: take its maximum first.  Later tiles exponentiate against
-        // the current reference at once and track their maximum on the side;
-        // the rare tile whose maximum passes the reference by more than
-        // kRescaleLog2 is redone against the new maximum (warp-uniformly,
-        // since P goes back to TMEM with warp-wide stores).  O, l and the
-        // exponent share the reference, so any choice is exact; p <= 2^8.
-        float m_use = m;
-        if (j == 0) {
+        float m_use = m, alpha = 1.0f, sum, tmax;
+        if constexpr (L::kSepP) {
+          // Separate P: the maximum first (no redo is possible once packed P
+          // waits in registers for its buffer), then the exponents.
           float acc[8];
 #pragma unroll
           for (int a = 0; a < 8; ++a) acc[a] = fmax3(s[2 * a], s[2 * a + 1], -INFINITY);
@@ -595,29 +731,76 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
 #pragma unroll
             for (int a = 0; a < 8; ++a) acc[a] = fmax3(acc[a], s[e + 2 * a], s[e + 2 * a + 1]);
           }
-          m_use = c * fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
-                            fmaxf(acc[6], acc[7]));
-          if (m_use == -INFINITY) m_use = 0.f;  // no allowed key in this row
-        }
-        FATTN_TRACE_EV(k, j, 8 * i + 3);
-        float tmax = -INFINITY;
-        float sum = exp_pass(s, m_use, s_addr, std::true_type{}, tmax);
-        float alpha = 1.0f;
-        if (j > 0) {
+          tmax = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
+                       fmaxf(acc[6], acc[7]));
           const float mxc = tmax * c;
           const bool move = mxc > m + kRescaleLog2;
-          if (__any_sync(0xffffffffu, move)) {
-            if (move) {
-              m_use = mxc;
-              alpha = ex2(m - m_use);
+          if (move) m_use = mxc;
+          if (m_use == -INFINITY) m_use = 0.f;  // no allowed key in this row yet
+          if (move && j > 0) alpha = ex2(m - m_use);
+          FATTN_TRACE_EV(k, j, 8 * i + 3);
+          uint32_t pk[kBN / 2];
+          sum = exp_pack(s, m_use, pk);
+          // P_i is free once the PV that read its previous contents is done
+          // (that PV also ends the last update of O_i before a rescale).
+          if (p_writes > 0) {
+            bool w_ok = ptx::mbar_wait(bar(L::bPVDone + i), (p_writes - 1) & 1, abort_flag, tmo);
+            w_ok = __all_sync(0xffffffffu, w_ok);
+            if (!w_ok) {
+              if (lane == 0) raise_error(p, abort_flag, kErrPipelineTimeout, kRoleSoftmax, L::bPVDone + i);
+              ok = false;
+              break;
             }
-            sum = exp_pass(s, m_use, s_addr, std::false_type{}, tmax);
+          }
+          ++p_writes;
+#pragma unroll
+          for (int ch = 0; ch < kBN / 32; ++ch) {
+            uint32_t part[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) part[e] = pk[ch * 16 + e];
+            ptx::tmem_st16(p_addr + ch * 16, part);
+          }
+        } else {
+          // Reference maximum m (log2 domain).  The first tile of a row has
+          // none yet: take its maximum first.  Later tiles exponentiate against
+          // the current reference at once and track their maximum on the side;
+          // the rare tile whose maximum passes the reference by more than
+          // kRescaleLog2 is redone against the new maximum (warp-uniformly,
+          // since P goes back to TMEM with warp-wide stores).  O, l and the
+          // exponent share the reference, so any choice is exact; p <= 2^8.
+          if (j == 0) {
+            float acc[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) acc[a] = fmax3(s[2 * a], s[2 * a + 1], -INFINITY);
+#pragma unroll
+            for (int e = 16; e < kBN; e += 16) {
+#pragma unroll
+              for (int a = 0; a < 8; ++a) acc[a] = fmax3(acc[a], s[e + 2 * a], s[e + 2 * a + 1]);
+            }
+            m_use = c * fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
+                              fmaxf(acc[6], acc[7]));
+            if (m_use == -INFINITY) m_use = 0.f;  // no allowed key in this row
+          }
+          FATTN_TRACE_EV(k, j, 8 * i + 3);
+          tmax = -INFINITY;
+          sum = exp_pass(s, m_use, s_addr, std::true_type{}, tmax);
+          if (j > 0) {
+            const float mxc = tmax * c;
+            const bool move = mxc > m + kRescaleLog2;
+            if (__any_sync(0xffffffffu, move)) {
+              if (move) {
+                m_use = mxc;
+                alpha = ex2(m - m_use);
+              }
+              sum = exp_pass(s, m_use, s_addr, std::false_type{}, tmax);
+            }
           }
         }
         // A row that moved its reference scales its O by exp2(m_old - m_new).
         // This warp owns these O rows (its TMEM lane quarter) and may touch
-        // them now: S_i(j) was issued after PV_i(j-1), so PV_i(j-1) has
-        // landed, and no MMA writes O_i until this warp reports P ready.
+        // them now: PV_i(j-1) has landed (with P aliasing S, S_i(j) was
+        // issued after it; with separate P, its completion was awaited
+        // above), and no MMA writes O_i until this warp reports P ready.
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           const uint32_t o_addr = tmem + ((uint32_t)(quarter * 32) << 16) + L::colO(i);
 #pragma unroll

@@ -101,19 +101,17 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// FATTN_WAIT_SPIN=1 polls with test_wait (no suspension) instead of try_wait.
-#ifndef FATTN_WAIT_SPIN
-#define FATTN_WAIT_SPIN 0
-#endif
-
 // Bounded wait: polls until the phase completes, the CTA-wide abort flag is
 // raised, or ``timeout_ns`` of wall time passes.  Returns false on the last
-// two.  No wait in this library is unbounded.
+// two.  No wait in this library is unbounded.  SPIN polls with test_wait
+// (never suspends: lowest wake-up latency, but it takes issue slots);
+// otherwise try_wait lets the hardware suspend the thread between polls.
+template <bool SPIN = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           const volatile int* abort_flag,
                                           uint64_t timeout_ns) {
   auto poll = [&]() {
-    return FATTN_WAIT_SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
+    return SPIN ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity);
   };
   if (poll()) return true;
   const uint64_t t0 = globaltimer_ns();

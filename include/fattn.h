@@ -57,7 +57,9 @@ enum fattn_status {
   FATTN_ERR_MISALIGNED = -3,       /* q/k/v/o not 16-byte aligned, lse not
                                       4-byte aligned */
   FATTN_ERR_TOO_LARGE = -4,        /* B*H*S rows exceed INT32_MAX */
-  FATTN_ERR_LAUNCH = -5,           /* the kernel launch itself failed */
+  FATTN_ERR_LAUNCH = -5,           /* the kernel launch failed, or (from
+                                      fattn_last_error) the kernel found its
+                                      shared memory base misaligned */
   FATTN_ERR_PIPELINE_TIMEOUT = -6, /* a device-side wait exceeded its limit */
   FATTN_ERR_CUDA = -7              /* another CUDA runtime/driver error */
 };
@@ -84,8 +86,9 @@ FATTN_API int fattn_fwd(const void *q, const void *k, const void *v, void *o,
 /*
  * Synchronises ``stream``, then reads and clears the current device's status
  * block.  Returns FATTN_OK, FATTN_ERR_PIPELINE_TIMEOUT (a kernel gave up on a
- * wait and unwound; its outputs are incomplete) or FATTN_ERR_CUDA when the
- * synchronisation itself reported an error.  ``detail`` (may be NULL)
+ * wait and unwound; its outputs are incomplete), FATTN_ERR_LAUNCH (a kernel
+ * did not run because its shared memory base was not 1024-byte aligned) or
+ * FATTN_ERR_CUDA when the synchronisation itself reported an error.  ``detail`` (may be NULL)
  * receives where the kernel error was raised: detail[0] = role << 8 |
  * barrier, detail[1] = block index.
  */
