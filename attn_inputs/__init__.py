@@ -194,3 +194,93 @@ WORKLOADS = {
     "s8192_d128_x4": Workload("B2_H16_S8192_D128_bf16_QKx4", 2, 16, 8192, 128,
                              "bf16", (False, True), 3, 4.0),
 }
+
+
+# --------------------------------------------------------------------------
+# New queries against a key/value cache ("FlashAttention V2", section 6:
+# inference with a KV cache).  Same generator; the cached lengths come from
+# the same SplitMix64 stream, far past the normals.
+# --------------------------------------------------------------------------
+
+_LENS_WORD0 = 1 << 40  # first stream word used for the cached lengths
+
+
+@dataclasses.dataclass
+class KVCache:
+    """One cache input set: ``q`` ``[B, H, Sq, D]``, ``k, v`` ``[B, H, Sk, D]``
+    (float32 holding ``dtype`` values) and ``lens`` (int64 ``[B]`` cached
+    lengths, or ``None`` for every length equal to ``Sk``)."""
+
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    lens: np.ndarray | None
+    dtype: str
+    seed: int
+
+
+def cache_lengths(seed: int, B: int, lo: int, hi: int) -> np.ndarray:
+    """``B`` lengths uniform in ``[lo, hi]`` from stream words 2**40 + b."""
+    if not 0 <= lo <= hi:
+        raise ValueError("need 0 <= lo <= hi")
+    w = splitmix64(seed, _LENS_WORD0, B)
+    return (np.uint64(lo) + w % np.uint64(hi - lo + 1)).astype(np.int64)
+
+
+def make_kvcache(B: int, H: int, Sq: int, Sk: int, D: int, dtype: str,
+                 seed: int, lens_range=None) -> KVCache:
+    """Q, then the K cache, then the V cache, i.i.d. N(0,1) from ``seed``;
+    ``lens_range = (lo, hi)`` draws per-batch cached lengths, else all
+    lengths are ``Sk``.  Cache rows past a batch's length hold normals too."""
+    if dtype not in DTYPES:
+        raise ValueError(f"unknown dtype {dtype!r}")
+    nq = B * H * Sq * D
+    nk = B * H * Sk * D
+    q = gaussian_tensor(seed, 0, (B, H, Sq, D), dtype)
+    k = gaussian_tensor(seed, nq, (B, H, Sk, D), dtype)
+    v = gaussian_tensor(seed, nq + nk, (B, H, Sk, D), dtype)
+    lens = None
+    if lens_range is not None:
+        lo, hi = lens_range
+        if hi > Sk:
+            raise ValueError("a cached length cannot exceed the capacity Sk")
+        lens = cache_lengths(seed, B, lo, hi)
+    return KVCache(q=q, k=k, v=v, lens=lens, dtype=dtype, seed=seed)
+
+
+@dataclasses.dataclass(frozen=True)
+class CacheWorkload:
+    name: str
+    B: int
+    H: int
+    Sq: int
+    Sk: int
+    D: int
+    dtype: str
+    causal: bool
+    seed: int
+    lens_range: tuple | None = None
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    def inputs(self) -> KVCache:
+        return make_kvcache(self.B, self.H, self.Sq, self.Sk, self.D,
+                            self.dtype, self.seed, self.lens_range)
+
+
+CACHE_WORKLOADS = {
+    # one new token per sequence, 16 sequences of mixed history length
+    "decode_b16_h16_d128_ragged": CacheWorkload(
+        "decode_B16_H16_Sq1_Sk16384_D128_bf16_lens1024-16384", 16, 16, 1,
+        16384, 128, "bf16", False, 40, (1024, 16384)),
+    # the long-sequence benchmark shape, one new token, full caches
+    "decode_b2_h16_s8192_d128": CacheWorkload(
+        "decode_B2_H16_Sq1_Sk8192_D128_bf16", 2, 16, 1, 8192, 128, "bf16",
+        False, 41),
+    # four new tokens per sequence under the causal mask, head dim 64, fp16
+    "decode_b8_h16_sq4_d64": CacheWorkload(
+        "decode_B8_H16_Sq4_Sk8192_D64_fp16_causal_lens1-8192", 8, 16, 4, 8192,
+        64, "fp16", True, 42, (1, 8192)),
+}

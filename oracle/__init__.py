@@ -18,6 +18,12 @@ Three independent statements of the same definition live here:
                          update of "FlashAttention V2" section 3; it checks the
                          algebra a tiled kernel relies on, not the kernel.
 
+Two more for attention of a few new queries against a key/value cache
+("FlashAttention V2", section 6: inference with a KV cache):
+
+* ``attn_kvcache``       -- the C oracle (``oracle_attn_kvcache``), fp64.
+* ``attn_kvcache_numpy`` -- the same definition in numpy fp64.
+
 Parity status: pinned.  The pins (closed forms, invariants, brute force at
 high precision) are in ``tests/test_oracle_pins.py``.
 """
@@ -59,6 +65,12 @@ def _load():
             ctypes.c_double, ctypes.POINTER(ctypes.c_longlong),
             ctypes.c_longlong, dp, dp, dp, ctypes.c_int]
         lib.oracle_attn_fwd.restype = ctypes.c_int
+        lib.oracle_attn_kvcache.argtypes = [
+            dp, dp, dp, ctypes.c_longlong, ctypes.c_longlong,
+            ctypes.c_longlong, ctypes.c_longlong, ctypes.c_longlong,
+            ctypes.POINTER(ctypes.c_longlong), ctypes.c_int, ctypes.c_double,
+            dp, dp, ctypes.c_int]
+        lib.oracle_attn_kvcache.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -183,3 +195,68 @@ def attn_fwd_online(q, k, v, causal: bool, scale: float, block_m: int = 128,
                 lse[b, h, i0:i1] = m + np.log(l)
     return o, lse
 
+
+
+def _lens_array(lens, B: int, Sk: int):
+    if lens is None:
+        return None
+    a = np.ascontiguousarray(np.asarray(lens, dtype=np.int64))
+    if a.shape != (B,):
+        raise ValueError("lens must have one entry per batch")
+    return a
+
+
+def attn_kvcache(q, k, v, causal: bool, scale: float, lens=None, threads=None):
+    """The C oracle for new queries against a cache.  ``q``: ``[B, H, Sq, D]``;
+    ``k, v``: ``[B, H, Sk, D]`` caches; ``lens``: cached length per batch
+    (``None``: all ``Sk``).  Query ``i`` is position ``len_b - Sq + i``; causal
+    keeps keys at or before that position.  Returns fp64 ``(O, LSE)``; a query
+    with no allowed key gets ``O = 0``, ``LSE = -inf``."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if q.ndim != 4 or k.shape != v.shape or k.ndim != 4:
+        raise ValueError("q must be [B, H, Sq, D]; k and v one [B, H, Sk, D]")
+    B, H, Sq, D = q.shape
+    if k.shape[:2] != (B, H) or k.shape[3] != D:
+        raise ValueError("q and the caches disagree on B, H or D")
+    Sk = k.shape[2]
+    la = _lens_array(lens, B, Sk)
+    o = np.empty((B, H, Sq, D), dtype=np.float64)
+    lse = np.empty((B, H, Sq), dtype=np.float64)
+    rc = _load().oracle_attn_kvcache(
+        _ptr(q), _ptr(k), _ptr(v), B, H, Sq, Sk, D,
+        None if la is None else la.ctypes.data_as(ctypes.POINTER(ctypes.c_longlong)),
+        int(bool(causal)), float(scale), _ptr(o), _ptr(lse),
+        int(threads or default_threads()))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_kvcache failed with code {rc}")
+    return o, lse
+
+
+def attn_kvcache_numpy(q, k, v, causal: bool, scale: float, lens=None):
+    """The cache definition in numpy fp64, one head at a time: scores of the
+    Sq queries against the first ``len_b`` cached keys, the causal mask
+    ``j <= len_b - Sq + i``, softmax, ``O = P V``; empty rows give 0 / -inf."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    la = _lens_array(lens, B, Sk)
+    o = np.zeros((B, H, Sq, D))
+    lse = np.full((B, H, Sq), -np.inf)
+    for b in range(B):
+        n = Sk if la is None else int(la[b])
+        if n == 0:
+            continue
+        pos = n - Sq + np.arange(Sq)
+        allowed = np.ones((Sq, n), dtype=bool)
+        if causal:
+            allowed = np.arange(n)[None, :] <= pos[:, None]
+        for h in range(H):
+            s = scale * (q[b, h] @ k[b, h, :n].T)
+            s = np.where(allowed, s, -np.inf)
+            rows = allowed.any(axis=1)
+            m = np.where(rows, s.max(axis=1, initial=-np.inf), 0.0)
+            e = np.exp(s - m[:, None])
+            l = e.sum(axis=1)
+            o[b, h, rows] = (e[rows] @ v[b, h, :n]) / l[rows, None]
+            lse[b, h, rows] = m[rows] + np.log(l[rows])
+    return o, lse

@@ -164,3 +164,139 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v,
   free(made);
   return status;
 }
+
+/*
+ * Attention of a few new query rows against a key/value cache
+ * ("FlashAttention V2", section 6, the table of when V2 is used: inference
+ * with a KV cache is served by its decoding variant).
+ *
+ * Head (b, h) holds len_b cached positions 0 .. len_b - 1 in rows of a
+ * [B, H, Sk, D] cache (Sk >= len_b is the cache's capacity; rows at or past
+ * len_b are ignored whatever they hold).  The Sq new queries are the last Sq
+ * positions of that sequence, so query i sits at position len_b - Sq + i.
+ * Allowed keys for query i: every j < len_b; with the causal mask only
+ * j <= len_b - Sq + i (the same "key <= query" rule as the self-attention
+ * case, positions counted from the start of the sequence).  Then, as above,
+ *
+ *   s_j = scale * q_i . k_j,  m = max s_j,  l = sum exp(s_j - m),
+ *   O_i = sum_j exp(s_j - m) v_j / l,  LSE_i = m + ln l.
+ *
+ * A query with no allowed key (len_b = 0, or causal with len_b - Sq + i < 0)
+ * gets O_i = 0 and LSE_i = -inf, the logarithm of an empty sum.
+ *
+ * q, o: [B, H, Sq, D]; k, v: [B, H, Sk, D]; lse: [B, H, Sq]; lens: [B] or
+ * NULL for len_b = Sk.  Every len_b must lie in [0, Sk].
+ */
+typedef struct {
+  const double *q, *k, *v;
+  const long long *lens;
+  long long H, Sq, Sk, D;
+  int causal;
+  double scale;
+  double *o, *lse;
+  long long r0, r1;
+  int status;
+} oracle_kv_job;
+
+static int oracle_kv_row(const oracle_kv_job *J, long long g, double *w) {
+  const long long Sq = J->Sq, Sk = J->Sk, D = J->D;
+  const long long bh = g / Sq, i = g % Sq, b = bh / J->H;
+  const long long len = J->lens ? J->lens[b] : Sk;
+  const double *qi = J->q + g * D;
+  const double *kh = J->k + bh * Sk * D;
+  const double *vh = J->v + bh * Sk * D;
+  double *oi = J->o + g * D;
+  long long n = len; /* keys 0 .. n-1 are allowed */
+  if (J->causal && len - Sq + i + 1 < n) n = len - Sq + i + 1;
+  for (long long d = 0; d < D; ++d) oi[d] = 0.0;
+  if (n <= 0) {
+    J->lse[g] = -INFINITY;
+    return ORACLE_OK;
+  }
+  for (long long j = 0; j < n; ++j) {
+    const double *kj = kh + j * D;
+    double acc = 0.0;
+    for (long long d = 0; d < D; ++d) acc += qi[d] * kj[d];
+    w[j] = J->scale * acc;
+  }
+  double m = w[0];
+  for (long long j = 1; j < n; ++j)
+    if (w[j] > m) m = w[j];
+  double l = 0.0;
+  for (long long j = 0; j < n; ++j) {
+    w[j] = exp(w[j] - m);
+    l += w[j];
+  }
+  if (!(l >= 1.0)) return ORACLE_ENORM;
+  for (long long j = 0; j < n; ++j) {
+    const double *vj = vh + j * D;
+    for (long long d = 0; d < D; ++d) oi[d] += w[j] * vj[d];
+  }
+  for (long long d = 0; d < D; ++d) oi[d] /= l;
+  J->lse[g] = m + log(l);
+  return ORACLE_OK;
+}
+
+static void *oracle_kv_worker(void *arg) {
+  oracle_kv_job *J = (oracle_kv_job *)arg;
+  double *w = (double *)malloc(sizeof(double) * (size_t)(J->Sk > 0 ? J->Sk : 1));
+  if (!w) {
+    J->status = ORACLE_ENOMEM;
+    return NULL;
+  }
+  for (long long r = J->r0; r < J->r1 && J->status == ORACLE_OK; ++r)
+    J->status = oracle_kv_row(J, r, w);
+  free(w);
+  return NULL;
+}
+
+int oracle_attn_kvcache(const double *q, const double *k, const double *v,
+                        long long B, long long H, long long Sq, long long Sk,
+                        long long D, const long long *lens, int causal,
+                        double scale, double *o, double *lse, int nthreads) {
+  if (!q || !k || !v || !o || !lse || B < 1 || H < 1 || Sq < 1 || Sk < 1 ||
+      D < 1)
+    return ORACLE_EINVAL;
+  if (!(scale > 0.0) || !isfinite(scale)) return ORACLE_EINVAL;
+  if (lens)
+    for (long long b = 0; b < B; ++b)
+      if (lens[b] < 0 || lens[b] > Sk) return ORACLE_EINVAL;
+  const long long total = B * H * Sq;
+  if (nthreads < 1) nthreads = 1;
+  if ((long long)nthreads > total) nthreads = (int)total;
+  oracle_kv_job *jobs =
+      (oracle_kv_job *)calloc((size_t)nthreads, sizeof(oracle_kv_job));
+  pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+  char *made = (char *)calloc((size_t)nthreads, 1);
+  if (!jobs || !tid || !made) {
+    free(jobs);
+    free(tid);
+    free(made);
+    return ORACLE_ENOMEM;
+  }
+  int status = ORACLE_OK;
+  for (int t = 0; t < nthreads; ++t) {
+    oracle_kv_job *J = &jobs[t];
+    J->q = q; J->k = k; J->v = v;
+    J->lens = lens;
+    J->H = H; J->Sq = Sq; J->Sk = Sk; J->D = D;
+    J->causal = causal;
+    J->scale = scale;
+    J->o = o; J->lse = lse;
+    J->r0 = total * t / nthreads;
+    J->r1 = total * (t + 1) / nthreads;
+    J->status = ORACLE_OK;
+    if (nthreads > 1 && pthread_create(&tid[t], NULL, oracle_kv_worker, J) == 0)
+      made[t] = 1;
+    else
+      oracle_kv_worker(J);
+  }
+  for (int t = 0; t < nthreads; ++t)
+    if (made[t]) pthread_join(tid[t], NULL);
+  for (int t = 0; t < nthreads; ++t)
+    if (jobs[t].status != ORACLE_OK) status = jobs[t].status;
+  free(jobs);
+  free(tid);
+  free(made);
+  return status;
+}

@@ -64,3 +64,22 @@ def test_sweep_seeds():
     assert (ws[3].S, ws[3].D, ws[3].dtype) == (512, 128, "bf16")
     assert (ws[-1].S, ws[-1].D, ws[-1].dtype) == (4097, 128, "bf16")
     assert all(w.B == 2 and w.H == 16 for w in ws)
+
+
+def test_cache_inputs_follow_the_stream():
+    """Q, then the K cache, then the V cache are consecutive normals of the
+    stream; lengths are reproducible and inside their range."""
+    x = ai.make_kvcache(2, 3, 4, 40, 8, "fp16", 77, (5, 40))
+    nq, nk = 2 * 3 * 4 * 8, 2 * 3 * 40 * 8
+    z = ai.round_to_dtype(ai.normals(77, 0, nq + 2 * nk), "fp16")
+    np.testing.assert_array_equal(x.q.reshape(-1), z[:nq])
+    np.testing.assert_array_equal(x.k.reshape(-1), z[nq:nq + nk])
+    np.testing.assert_array_equal(x.v.reshape(-1), z[nq + nk:])
+    assert x.lens.dtype == np.int64 and x.lens.shape == (2,)
+    assert ((x.lens >= 5) & (x.lens <= 40)).all()
+    np.testing.assert_array_equal(x.lens, ai.cache_lengths(77, 2, 5, 40))
+    many = ai.cache_lengths(1, 4000, 3, 9)
+    assert set(np.unique(many).tolist()) == set(range(3, 10))
+    assert ai.make_kvcache(1, 1, 1, 4, 8, "bf16", 1).lens is None
+    with pytest.raises(ValueError):
+        ai.make_kvcache(1, 1, 1, 4, 8, "bf16", 1, (1, 5))
