@@ -6,6 +6,7 @@ kernels of that library; there is no other implementation to fall back to, and
 calling into a missing library raises.
 
     o, lse = forward(q, k, v, causal=True)      # torch tensors on a GB300
+    o, lse = forward_kvcache(q_new, k_cache, v_cache, cache_lens)  # decoding
 
 ``q, k, v``: contiguous ``[B, H, S, D]`` fp16 or bf16 CUDA tensors, D in
 {64, 128}.  Returns ``o`` (same shape and dtype) and ``lse`` (``[B, H, S]``
@@ -61,6 +62,13 @@ def lib() -> ctypes.CDLL:
         l.fattn_error_string.restype = ctypes.c_char_p
         l.fattn_plan.argtypes = [i, i, i, i, i, ip, ip, ip, ip, ip, ip]
         l.fattn_plan.restype = i
+        u64 = ctypes.c_ulonglong
+        l.fattn_fwd_kvcache.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i,
+                                        i, f, i, vp, u64, vp]
+        l.fattn_fwd_kvcache.restype = i
+        l.fattn_kvcache_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(u64),
+                                         ip, ip, ip, ip]
+        l.fattn_kvcache_plan.restype = i
         l.fattn_version.argtypes = []
         l.fattn_version.restype = i
         _lib = l
@@ -95,6 +103,31 @@ def fattn_plan(B, H, S, D, causal=False) -> dict:
     keys = ("grid", "block", "smem_bytes", "units", "q_tiles_per_unit",
             "kv_stages")
     return {k_: x.value for k_, x in zip(keys, vals)}
+
+
+def fattn_fwd_kvcache(q, k_cache, v_cache, cache_lens, o, lse, B, H, Sq, Sk,
+                      D, causal, scale, dtype, workspace, workspace_bytes,
+                      stream) -> int:
+    """``fattn_fwd_kvcache`` with integer device pointers (``cache_lens`` may
+    be 0 for every length equal to ``Sk``) and an integer stream."""
+    return lib().fattn_fwd_kvcache(q, k_cache, v_cache, cache_lens or None, o,
+                                   lse, B, H, Sq, Sk, D, int(causal),
+                                   float(scale), dtype, workspace,
+                                   int(workspace_bytes), stream)
+
+
+def fattn_kvcache_plan(B, H, Sq, Sk, D) -> dict:
+    """The launch ``fattn_fwd_kvcache`` would make on the current device."""
+    ws = ctypes.c_ulonglong()
+    vals = [ctypes.c_int() for _ in range(4)]
+    rc = lib().fattn_kvcache_plan(B, H, Sq, Sk, D, ctypes.byref(ws),
+                                  *[ctypes.byref(x) for x in vals])
+    if rc != FATTN_OK:
+        raise FattnError(rc, "fattn_kvcache_plan")
+    out = {"workspace_bytes": ws.value}
+    out.update({k_: x.value for k_, x in
+                zip(("grid", "block", "smem_bytes", "split_warps"), vals)})
+    return out
 
 
 def fattn_version() -> int:
@@ -141,4 +174,55 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None,
                    stream.cuda_stream)
     if rc != FATTN_OK:
         raise FattnError(rc)
+    return out, lse
+
+
+def forward_kvcache(q, k_cache, v_cache, cache_lens=None, causal: bool = False,
+                    scale: float | None = None, out=None, lse=None,
+                    workspace=None, stream=None):
+    """Attention of ``Sq`` new queries against a key/value cache.
+
+    ``q``: contiguous ``[B, H, Sq, D]`` (Sq <= 16); ``k_cache, v_cache``:
+    contiguous ``[B, H, Sk, D]`` of the same dtype; ``cache_lens``: optional
+    int32 CUDA tensor ``[B]`` of cached lengths (default: all ``Sk``).  Query
+    ``i`` sits at position ``len_b - Sq + i``; ``causal`` keeps keys up to it.
+    ``workspace``: optional uint8 CUDA tensor of at least
+    ``fattn_kvcache_plan(...)["workspace_bytes"]`` bytes (allocated here if
+    absent).  Returns ``(o, lse)``; raises FattnError on a non-zero status."""
+    import torch
+    if q.dim() != 4 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("q must be [B, H, Sq, D]; caches one [B, H, Sk, D]")
+    B, H, Sq, D = q.shape
+    if k_cache.shape[0] != B or k_cache.shape[1] != H or k_cache.shape[3] != D:
+        raise ValueError("q and the caches disagree on B, H or D")
+    Sk = k_cache.shape[2]
+    for t in (q, k_cache, v_cache):
+        if not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q and the caches must be contiguous CUDA tensors")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("q and the caches must share a dtype")
+    lens_ptr = 0
+    if cache_lens is not None:
+        if (cache_lens.dtype != torch.int32 or cache_lens.shape != (B,)
+                or not cache_lens.is_contiguous() or not cache_lens.is_cuda):
+            raise ValueError("cache_lens must be a contiguous int32 CUDA tensor [B]")
+        lens_ptr = cache_lens.data_ptr()
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = fattn_kvcache_plan(B, H, Sq, Sk, D)["workspace_bytes"]
+        workspace = torch.empty(max(16, need), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    rc = fattn_fwd_kvcache(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                           lens_ptr, out.data_ptr(), lse.data_ptr(), B, H, Sq,
+                           Sk, D, causal, scale, _dtype_code(q),
+                           workspace.data_ptr(), workspace.numel(),
+                           stream.cuda_stream)
+    if rc != FATTN_OK:
+        raise FattnError(rc, "fattn_fwd_kvcache")
     return out, lse

@@ -1,7 +1,7 @@
 """Build ``libfattn.so`` in-tree with nvcc for sm_103a.
 
-The translation units compile in parallel (one per head dim plus the host
-library) and are linked into one shared library with the CUDA runtime linked
+The translation units compile in parallel (one per head dim and kernel
+family, plus the host library) and are linked into one shared library with the CUDA runtime linked
 statically, so the library loads on machines without a GPU driver.
 
     python -m exact_attention_forward_10_gb300.build [--verbose]
@@ -24,7 +24,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libfattn.so")
 
-SOURCES = ["fattn_api.cu", "fattn_fwd_d64.cu", "fattn_fwd_d128.cu"]
+SOURCES = ["fattn_api.cu", "fattn_fwd_d64.cu", "fattn_fwd_d128.cu",
+           "fattn_decode.cu", "fattn_decode_d64.cu", "fattn_decode_d128.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "fattn.h"
+#include "fattn_decode_launch.h"
 #include "fattn_launch.cuh"
 #include "fattn_status.h"
 
@@ -161,6 +162,52 @@ int encode_bhsd(CUtensorMap* tm, const void* ptr, int S, int BH, int D,
   return r == CUDA_SUCCESS ? kOk : kErrCuda;
 }
 
+// The K or V cache [BH, Sk, D] for the split decode kernel: boxes of 64
+// columns x 32 rows (one key per lane), 128-byte swizzle.
+int encode_cache(CUtensorMap* tm, const void* ptr, int Sk, int BH, int D,
+                 bool bf16) {
+  const DriverFns& f = driver();
+  if (!f.encode) return kErrCuda;
+  cuuint64_t gdim[3] = {(cuuint64_t)D, (cuuint64_t)Sk, (cuuint64_t)BH};
+  cuuint64_t gstride[2] = {(cuuint64_t)D * 2, (cuuint64_t)Sk * (cuuint64_t)D * 2};
+  cuuint32_t box[3] = {(cuuint32_t)decode::kBoxCols, (cuuint32_t)decode::kTileKeys, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = f.encode(
+      tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+      3, const_cast<void*>(ptr), gdim, gstride, box, estride,
+      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? kOk : kErrCuda;
+}
+
+struct KvPlan {
+  int grid, warps, threads, smem, split_warps;
+  unsigned long long records, ws_bytes;
+};
+
+// Sizes-only checks and the launch shape of the cache-attention kernels on a
+// device with ``sms`` SMs: one split CTA per SM, fewer when the caches hold
+// fewer tiles than the CTAs have warps.
+int kvcache_checks(int B, int H, int Sq, int Sk, int D, int sms, KvPlan* plan) {
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return kErrInvalidArg;
+  if (D != 64 && D != 128) return kErrUnsupported;
+  if (Sq > decode::kMaxSq) return kErrUnsupported;
+  const long long bh = (long long)B * H;
+  if (bh * Sq > INT_MAX || bh * Sk > INT_MAX) return kErrTooLarge;
+  plan->warps = decode::warps_per_cta(D, Sq);
+  plan->threads = plan->warps * 32;
+  plan->smem = decode::smem_bytes(D, Sq);
+  const long long max_tiles = bh * ((Sk + decode::kTileKeys - 1) / decode::kTileKeys);
+  long long grid = (max_tiles + plan->warps - 1) / plan->warps;
+  if (grid > sms) grid = sms;
+  if (grid < 1) grid = 1;
+  plan->grid = (int)grid;
+  plan->split_warps = plan->grid * plan->warps;
+  plan->records = (unsigned long long)plan->split_warps + (unsigned long long)bh;
+  plan->ws_bytes = plan->records * (unsigned long long)Sq * (unsigned long long)(D + 1) * 4ull;
+  return kOk;
+}
+
 struct Plan {
   int qt, ns, threads, smem, units_per_head, total_units;
 };
@@ -293,6 +340,112 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o,
   const cudaError_t e = D == 64 ? launch_fwd_d64(causal != 0, bf16, a)
                                 : launch_fwd_d128(causal != 0, bf16, a);
   if (e != cudaSuccess) {
+    cudaGetLastError();
+    return FATTN_ERR_LAUNCH;
+  }
+  return FATTN_OK;
+}
+
+FATTN_API int fattn_kvcache_plan(int B, int H, int Sq, int Sk, int D,
+                                 unsigned long long* workspace_bytes, int* grid,
+                                 int* block, int* smem_bytes, int* split_warps) {
+  DeviceState* ds = nullptr;
+  int rc = current_device(&ds, nullptr);
+  if (rc != kOk) return rc;
+  KvPlan plan;
+  rc = kvcache_checks(B, H, Sq, Sk, D, ds->sms, &plan);
+  if (rc != kOk) return rc;
+  if (workspace_bytes) *workspace_bytes = plan.ws_bytes;
+  if (grid) *grid = plan.grid;
+  if (block) *block = plan.threads;
+  if (smem_bytes) *smem_bytes = plan.smem;
+  if (split_warps) *split_warps = plan.split_warps;
+  return kOk;
+}
+
+FATTN_API int fattn_fwd_kvcache(const void* q, const void* k_cache,
+                                const void* v_cache, const int* cache_lens,
+                                void* o, float* lse, int B, int H, int Sq,
+                                int Sk, int D, int causal, float scale,
+                                int dtype, void* workspace,
+                                unsigned long long workspace_bytes,
+                                fattn_stream_t stream) {
+  // ---- host-side checks, nothing enqueued yet
+  if (!q || !k_cache || !v_cache || !o || !lse || !workspace)
+    return FATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return FATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FATTN_ERR_UNSUPPORTED;
+  if (Sq > decode::kMaxSq) return FATTN_ERR_UNSUPPORTED;
+  if (dtype != FATTN_FP16 && dtype != FATTN_BF16) return FATTN_ERR_UNSUPPORTED;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) |
+                        reinterpret_cast<uintptr_t>(k_cache) |
+                        reinterpret_cast<uintptr_t>(v_cache) |
+                        reinterpret_cast<uintptr_t>(o) |
+                        reinterpret_cast<uintptr_t>(workspace);
+  if ((a16 & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0)
+    return FATTN_ERR_MISALIGNED;
+
+  DeviceState* ds = nullptr;
+  int dev = 0;
+  int rc = current_device(&ds, &dev);
+  if (rc != kOk) return rc;
+  KvPlan plan;
+  rc = kvcache_checks(B, H, Sq, Sk, D, ds->sms, &plan);
+  if (rc != kOk) return rc;
+  if (workspace_bytes < plan.ws_bytes) return FATTN_ERR_INVALID_ARG;
+
+  const size_t bh = (size_t)B * H;
+  const size_t qbytes = bh * Sq * D * 2;
+  const size_t cbytes = bh * Sk * D * 2;
+  const size_t lbytes = bh * Sq * sizeof(float);
+  const size_t nbytes = cache_lens ? (size_t)B * sizeof(int) : 0;
+  const size_t wbytes = (size_t)plan.ws_bytes;
+  const void* ins[4] = {q, k_cache, v_cache, cache_lens};
+  const size_t insz[4] = {qbytes, cbytes, cbytes, nbytes};
+  const void* outs[3] = {o, lse, workspace};
+  const size_t outsz[3] = {qbytes, lbytes, wbytes};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 4; ++j)
+      if (insz[j] && overlaps(outs[i], outsz[i], ins[j], insz[j]))
+        return FATTN_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlaps(outs[i], outsz[i], outs[j], outsz[j])) return FATTN_ERR_INVALID_ARG;
+  }
+  for (int j = 0; j < 4; ++j)
+    if (insz[j] && (rc = check_device_buffer(ins[j], insz[j], dev)) != kOk) return rc;
+  for (int i = 0; i < 3; ++i)
+    if ((rc = check_device_buffer(outs[i], outsz[i], dev)) != kOk) return rc;
+
+  const bool bf16 = dtype == FATTN_BF16;
+  CUtensorMap tm_k, tm_v;
+  if (encode_cache(&tm_k, k_cache, Sk, (int)bh, D, bf16) != kOk ||
+      encode_cache(&tm_v, v_cache, Sk, (int)bh, D, bf16) != kOk)
+    return FATTN_ERR_CUDA;
+
+  decode::DecodeLaunch a;
+  a.tm_k = &tm_k;
+  a.tm_v = &tm_v;
+  decode::DecodeParams& p = a.params;
+  p.q = q;
+  p.lens = cache_lens;
+  p.part_o = static_cast<float*>(workspace);
+  p.part_lse = static_cast<float*>(workspace) + plan.records * (size_t)Sq * D;
+  p.o = o;
+  p.lse = lse;
+  p.status = ds->status;
+  p.B = B;
+  p.H = H;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.causal = causal != 0;
+  p.n_warps = plan.split_warps;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.timeout_ns = wait_timeout_ns();
+  a.grid = plan.grid;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  if (decode::launch(D, bf16, a) != cudaSuccess) {
     cudaGetLastError();
     return FATTN_ERR_LAUNCH;
   }

@@ -1,0 +1,67 @@
+// Host-side interface of the cache-attention kernels (fattn_decode.cu), used by
+// the C ABI in fattn_api.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fattn_decode.cuh"
+
+namespace fattn {
+namespace decode {
+
+struct DecodeLaunch {
+  const CUtensorMap* tm_k;  // K cache, [BH, Sk, D], boxes of 64 cols x 32 rows
+  const CUtensorMap* tm_v;  // V cache, same geometry
+  DecodeParams params;
+  int grid;                 // CTAs of the split kernel (one per SM)
+  cudaStream_t stream;
+};
+
+// The compiled query-count bucket (1, 4 or 16) that serves Sq new queries.
+int sq_bucket(int Sq);
+// Warps per split CTA and its dynamic shared memory, for head dim D.
+int warps_per_cta(int D, int Sq);
+int smem_bytes(int D, int Sq);
+// Enqueue the split kernel and then the merge kernel on a.stream.
+cudaError_t launch(int D, bool bf16, const DecodeLaunch& a);
+// Per head dim, defined in fattn_decode_d64.cu / fattn_decode_d128.cu.
+cudaError_t launch_d64(bool bf16, const DecodeLaunch& a);
+cudaError_t launch_d128(bool bf16, const DecodeLaunch& a);
+
+template <int D, int SQ, bool BF16>
+cudaError_t launch_split(const DecodeLaunch& a) {
+  using L = DecodeLayout<D, SQ>;
+  auto kern = &fattn_decode_kernel<D, SQ, BF16>;
+  static volatile bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             L::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set[dev] = true;
+  }
+  kern<<<a.grid, L::kThreads, L::kSmemBytes, a.stream>>>(*a.tm_k, *a.tm_v, a.params);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long rows = (long long)a.params.B * a.params.H * a.params.Sq;
+  const int blocks = (int)((rows + kCombineWarps - 1) / kCombineWarps);
+  fattn_decode_combine_kernel<D, BF16>
+      <<<blocks, kCombineWarps * 32, 0, a.stream>>>(a.params);
+  return cudaGetLastError();
+}
+
+template <int D, bool BF16>
+cudaError_t launch_d(const DecodeLaunch& a) {
+  switch (sq_bucket(a.params.Sq)) {
+    case 1: return launch_split<D, 1, BF16>(a);
+    case 4: return launch_split<D, 4, BF16>(a);
+    default: return launch_split<D, 16, BF16>(a);
+  }
+}
+
+
+}  // namespace decode
+}  // namespace fattn

@@ -53,7 +53,8 @@ enum fattn_status {
                                       overlapping buffers, non-device memory
                                       or a buffer smaller than its tensor */
   FATTN_ERR_UNSUPPORTED = -2,      /* D not in {64, 128}, unknown dtype, no
-                                      CUDA device, or device is not sm_103 */
+                                      CUDA device, device is not sm_103, or
+                                      (cache attention) Sq > 16 */
   FATTN_ERR_MISALIGNED = -3,       /* q/k/v/o not 16-byte aligned, lse not
                                       4-byte aligned */
   FATTN_ERR_TOO_LARGE = -4,        /* B*H*S rows exceed INT32_MAX */
@@ -87,8 +88,10 @@ FATTN_API int fattn_fwd(const void *q, const void *k, const void *v, void *o,
  * Synchronises ``stream``, then reads and clears the current device's status
  * block.  Returns FATTN_OK, FATTN_ERR_PIPELINE_TIMEOUT (a kernel gave up on a
  * wait and unwound; its outputs are incomplete), FATTN_ERR_LAUNCH (a kernel
- * did not run because its shared memory base was not 1024-byte aligned) or
- * FATTN_ERR_CUDA when the synchronisation itself reported an error.  ``detail`` (may be NULL)
+ * did not run because its shared memory base was not 1024-byte aligned),
+ * FATTN_ERR_INVALID_ARG (fattn_fwd_kvcache met a cached length outside
+ * [0, Sk]) or FATTN_ERR_CUDA when the synchronisation itself reported an
+ * error.  ``detail`` (may be NULL)
  * receives where the kernel error was raised: detail[0] = role << 8 |
  * barrier, detail[1] = block index.
  */
@@ -109,6 +112,75 @@ FATTN_API const char *fattn_error_string(int status);
 FATTN_API int fattn_plan(int B, int H, int S, int D, int causal, int *grid,
                          int *block, int *smem_bytes, int *units,
                          int *q_tiles_per_unit, int *kv_stages);
+
+/*
+ * Attention of a few new queries against a key/value cache ("FlashAttention
+ * V2", section 6: inference with a KV cache, which FlashAttention serves with
+ * its decoding variant; the per-row recurrence of section 3).
+ *
+ * For batch b, head h: the cache holds len_b positions (rows 0 .. len_b-1 of
+ * the [B, H, Sk, D] caches; Sk is the capacity, rows at or past len_b are
+ * ignored whatever they hold).  The Sq new queries are the last Sq positions
+ * of the sequence: query i sits at position len_b - Sq + i and attends to
+ * every key j < len_b, or with causal != 0 only to j <= len_b - Sq + i.
+ *   O[b,h,i,:] = sum_j softmax_j(scale * q_i . k_j) V[b,h,j,:]
+ *   LSE[b,h,i] = m + ln(sum_j exp(s_ij - m))
+ * A query with no allowed key (len_b = 0, or causal with len_b < Sq - i)
+ * gets O = 0 and LSE = -inf.
+ *
+ * The keys are split across every warp of the GPU; each slice writes a
+ * partial (O, LSE) record to ``workspace`` and a second kernel merges a
+ * head's records with weights exp(LSE_s - max LSE).  Both kernels are
+ * enqueued on ``stream``.
+ *
+ *   q          device [B, H, Sq, D] 16-bit, 16-byte aligned
+ *   k_cache    device [B, H, Sk, D] 16-bit, 16-byte aligned
+ *   v_cache    device [B, H, Sk, D] 16-bit, 16-byte aligned
+ *   cache_lens device int32 [B] cached lengths in [0, Sk], 4-byte aligned, or
+ *              NULL for every length equal to Sk.  A value outside [0, Sk]
+ *              is clamped for memory safety and reported by
+ *              fattn_last_error as FATTN_ERR_INVALID_ARG (detail[0] = 6 << 8,
+ *              detail[1] = the batch index); the outputs are then undefined.
+ *   o          device [B, H, Sq, D] 16-bit output, 16-byte aligned
+ *   lse        device [B, H, Sq] fp32 output, 4-byte aligned
+ *   B, H       batch and heads (>= 1)
+ *   Sq         new queries per head: 1 .. 16
+ *   Sk         cache capacity (>= 1)
+ *   D          head dimension: 64 or 128
+ *   causal     0: every cached key; non-zero: keys up to each query's position
+ *   scale      score multiplier, finite and > 0
+ *   dtype      FATTN_FP16 or FATTN_BF16 (q, caches and o)
+ *   workspace  device scratch of at least the size fattn_kvcache_plan gives
+ *              for these sizes on the current device, 16-byte aligned; owned
+ *              by the caller; its contents need no initialisation and are
+ *              meaningless afterwards.  Calls in flight at the same time need
+ *              separate workspaces.
+ *   workspace_bytes  its size in bytes
+ * Outputs (o, lse, workspace) may not overlap the inputs or each other.
+ * Returns FATTN_OK once both kernels are enqueued, else a negative status
+ * (FATTN_ERR_UNSUPPORTED for Sq > 16 or D not in {64, 128};
+ * FATTN_ERR_INVALID_ARG also for a workspace that is too small).
+ */
+FATTN_API int fattn_fwd_kvcache(const void *q, const void *k_cache,
+                                const void *v_cache, const int *cache_lens,
+                                void *o, float *lse, int B, int H, int Sq,
+                                int Sk, int D, int causal, float scale,
+                                int dtype, void *workspace,
+                                unsigned long long workspace_bytes,
+                                fattn_stream_t stream);
+
+/*
+ * The launch fattn_fwd_kvcache would make for these sizes on the current
+ * device, without launching.  Fills (each pointer may be NULL): the
+ * workspace bytes it needs, the split kernel's grid (CTAs), block (threads)
+ * and dynamic shared memory, and the total number of split warps.  Needs a
+ * device (the split depends on its SM count).  Returns FATTN_OK or the
+ * status fattn_fwd_kvcache would return for the same sizes.
+ */
+FATTN_API int fattn_kvcache_plan(int B, int H, int Sq, int Sk, int D,
+                                 unsigned long long *workspace_bytes,
+                                 int *grid, int *block, int *smem_bytes,
+                                 int *split_warps);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 FATTN_API int fattn_version(void);

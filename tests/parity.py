@@ -111,3 +111,64 @@ def check_sampled(x: attn_inputs.QKV, causal: bool, seed: int, label: str = "",
     ro, rl = oracle.attn_fwd(x.q, x.k, x.v, causal, scale, rows=rows)
     return compare(o.reshape(-1, D)[rows], lse.reshape(-1)[rows], ro, rl,
                    x.dtype, label)
+
+
+# ------------------------------------------------ attention against a cache
+
+def run_cuda_kvcache(x: attn_inputs.KVCache, causal: bool, scale: float,
+                     lens=None, poison: bool = True, workspace=None,
+                     stale_nan: bool = False):
+    """The cache path through the C ABI; outputs as fp64 numpy arrays.
+    ``stale_nan`` fills every cache row at or past its batch's length with
+    NaN before the call (those rows must not matter)."""
+    import torch
+
+    import exact_attention_forward_10_gb300 as fattn
+
+    dev = torch.device("cuda:0")
+    tdt = torch_dtype(x.dtype)
+    q, k, v = (torch.from_numpy(a).to(dev).to(tdt) for a in (x.q, x.k, x.v))
+    if lens is None:
+        lens = x.lens
+    lt = None
+    if lens is not None:
+        lt = torch.as_tensor(np.asarray(lens), dtype=torch.int32, device=dev)
+        if stale_nan:
+            for b, n in enumerate(np.asarray(lens).tolist()):
+                k[b, :, n:] = float("nan")
+                v[b, :, n:] = float("nan")
+    B, H, Sq, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev)
+    if poison:
+        o.fill_(float("nan"))
+        lse.fill_(float("nan"))
+    fattn.forward_kvcache(q, k, v, lt, causal=causal, scale=scale, out=o,
+                          lse=lse, workspace=workspace)
+    torch.cuda.synchronize()
+    rc, where = fattn.fattn_last_error(0)
+    assert rc == 0, f"kernel status {rc} ({fattn.fattn_error_string(rc)}) at {where}"
+    return o.double().cpu().numpy(), lse.double().cpu().numpy()
+
+
+def compare_kvcache(o, lse, ro, rl, dtype: str, label: str = ""):
+    """Parity for the cache path: rows with no allowed key must be exactly
+    O = 0 and LSE = -inf; every other element as in ``compare``."""
+    assert not np.isnan(o).any(), f"{label}: NaN (unwritten?) O"
+    assert not np.isnan(lse).any(), f"{label}: NaN (unwritten?) LSE"
+    empty = np.isneginf(rl)
+    np.testing.assert_array_equal(np.isneginf(lse), empty,
+                                  err_msg=f"{label}: empty-row pattern")
+    assert np.all(o[empty] == 0.0), f"{label}: empty rows must be zero"
+    full = ~empty
+    return compare(o[full], lse[full], ro[full], rl[full], dtype, label)
+
+
+def check_kvcache(x: attn_inputs.KVCache, causal: bool, label: str = "",
+                  stale_nan: bool = False):
+    """Every element of the cache path against the fp64 cache oracle."""
+    D = x.q.shape[-1]
+    scale = 1.0 / math.sqrt(D)
+    o, lse = run_cuda_kvcache(x, causal, scale, stale_nan=stale_nan)
+    ro, rl = oracle.attn_kvcache(x.q, x.k, x.v, causal, scale, x.lens)
+    return compare_kvcache(o, lse, ro, rl, x.dtype, label)

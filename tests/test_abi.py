@@ -89,3 +89,37 @@ def test_plan_without_device(lib):
     assert 1 <= p["grid"] <= p["units"]
     with pytest.raises(fattn.FattnError):
         fattn.fattn_plan(1, 1, 10, 80)
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(q=0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(k=0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(ws=0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(lse=0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(B=0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(Sq=0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(Sk=0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(Sq=17), fattn.FATTN_ERR_UNSUPPORTED),
+    (dict(D=256), fattn.FATTN_ERR_UNSUPPORTED),
+    (dict(dtype=5), fattn.FATTN_ERR_UNSUPPORTED),
+    (dict(q=P + 4), fattn.FATTN_ERR_MISALIGNED),
+    (dict(v=P * 7 + 8), fattn.FATTN_ERR_MISALIGNED),
+    (dict(ws=P * 13 + 8), fattn.FATTN_ERR_MISALIGNED),
+    (dict(lse=P * 11 + 1), fattn.FATTN_ERR_MISALIGNED),
+    (dict(lens=P * 15 + 2), fattn.FATTN_ERR_MISALIGNED),
+])
+def test_kvcache_host_side_rejections(lib, args, want):
+    """Argument errors of the cache entry point are found before any CUDA
+    call (workspace size and overlap checks need the device's SM count and
+    are covered by the GPU tests)."""
+    a = dict(q=P, k=P * 3, v=P * 7, lens=P * 15, o=P * 9, lse=P * 11, B=2, H=4,
+             Sq=1, Sk=4096, D=128, causal=0, scale=0.125, dtype=1, ws=P * 13,
+             ws_bytes=1 << 30, stream=0)
+    a.update(args)
+    rc = fattn.fattn_fwd_kvcache(a["q"], a["k"], a["v"], a["lens"], a["o"],
+                                 a["lse"], a["B"], a["H"], a["Sq"], a["Sk"],
+                                 a["D"], a["causal"], a["scale"], a["dtype"],
+                                 a["ws"], a["ws_bytes"], a["stream"])
+    assert rc == want
