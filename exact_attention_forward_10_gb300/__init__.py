@@ -69,6 +69,9 @@ def lib() -> ctypes.CDLL:
         l.fattn_kvcache_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(u64),
                                          ip, ip, ip, ip]
         l.fattn_kvcache_plan.restype = i
+        l.fattn_fwd_kvcache_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i,
+                                                i, i, i, i, f, i, vp, vp]
+        l.fattn_fwd_kvcache_noalloc.restype = i
         l.fattn_version.argtypes = []
         l.fattn_version.restype = i
         _lib = l
@@ -114,6 +117,16 @@ def fattn_fwd_kvcache(q, k_cache, v_cache, cache_lens, o, lse, B, H, Sq, Sk,
                                    lse, B, H, Sq, Sk, D, int(causal),
                                    float(scale), dtype, workspace,
                                    int(workspace_bytes), stream)
+
+
+def fattn_fwd_kvcache_noalloc(q, k_cache, v_cache, cache_lens, o, lse, B, H,
+                              Sq, Sk, D, causal, scale, dtype, status_words,
+                              stream) -> int:
+    """``fattn_fwd_kvcache_noalloc`` with integer device pointers
+    (``cache_lens`` and ``status_words`` may be 0) and an integer stream."""
+    return lib().fattn_fwd_kvcache_noalloc(
+        q, k_cache, v_cache, cache_lens or None, o, lse, B, H, Sq, Sk, D,
+        int(causal), float(scale), dtype, status_words or None, stream)
 
 
 def fattn_kvcache_plan(B, H, Sq, Sk, D) -> dict:

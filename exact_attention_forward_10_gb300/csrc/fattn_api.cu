@@ -236,6 +236,62 @@ int host_checks(int B, int H, int S, int D, Plan* plan) {
   return kOk;
 }
 
+// ---- the allocation-free cache entry: scratch and status in static device
+// arrays, device state kept without the status-block allocation
+
+__device__ __align__(256) static unsigned char g_noalloc_scratch[FATTN_NOALLOC_SCRATCH_BYTES];
+__device__ __align__(16) static int g_noalloc_status[kStatusWords];
+
+struct NoAllocState {
+  bool init = false;
+  bool supported = false;
+  int sms = 0;
+  void* scratch = nullptr;  // device address of g_noalloc_scratch
+  int* status = nullptr;    // device address of g_noalloc_status
+};
+
+NoAllocState g_noalloc[kMaxDevices];
+
+// The current device's no-alloc state, set up on its first use: attribute
+// queries and the symbols' device addresses (no allocation).
+int noalloc_device(NoAllocState** out, int* dev_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return kErrUnsupported;
+  }
+  if (dev < 0 || dev >= kMaxDevices) return kErrUnsupported;
+  std::lock_guard<std::mutex> lock(g_mu);
+  NoAllocState& d = g_noalloc[dev];
+  if (!d.init) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return kErrCuda;
+    }
+    d.sms = sms;
+    d.supported = (major == 10 && minor == 3);
+    if (d.supported) {
+      void* scratch = nullptr;
+      void* status = nullptr;
+      if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess ||
+          cudaGetSymbolAddress(&status, g_noalloc_status) != cudaSuccess) {
+        cudaGetLastError();
+        return kErrCuda;
+      }
+      d.scratch = scratch;
+      d.status = static_cast<int*>(status);
+    }
+    d.init = true;
+  }
+  if (!d.supported) return kErrUnsupported;
+  *out = &d;
+  if (dev_out) *dev_out = dev;
+  return kOk;
+}
+
 }  // namespace
 }  // namespace fattn
 
@@ -471,6 +527,95 @@ FATTN_API int fattn_last_error(fattn_stream_t stream, int* detail) {
     detail[1] = h[2];
   }
   return h[0];
+}
+
+FATTN_API int fattn_fwd_kvcache_noalloc(const void* q, const void* k_cache,
+                                        const void* v_cache, const int* cache_lens,
+                                        void* o, float* lse, int B, int H, int Sq,
+                                        int Sk, int D, int causal, float scale,
+                                        int dtype, int* status_words,
+                                        fattn_stream_t stream) {
+  // ---- host-side checks, nothing enqueued yet
+  if (!q || !k_cache || !v_cache || !o || !lse) return FATTN_ERR_INVALID_ARG;
+  if (!(scale > 0.0f) || !std::isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Sq < 1 || Sk < 1) return FATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FATTN_ERR_UNSUPPORTED;
+  if (Sq > decode::kMaxSq) return FATTN_ERR_UNSUPPORTED;
+  if (dtype != FATTN_FP16 && dtype != FATTN_BF16) return FATTN_ERR_UNSUPPORTED;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) |
+                        reinterpret_cast<uintptr_t>(k_cache) |
+                        reinterpret_cast<uintptr_t>(v_cache) |
+                        reinterpret_cast<uintptr_t>(o);
+  if ((a16 & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(cache_lens) & 3u) != 0 ||
+      (reinterpret_cast<uintptr_t>(status_words) & 3u) != 0)
+    return FATTN_ERR_MISALIGNED;
+
+  NoAllocState* ds = nullptr;
+  int dev = 0;
+  int rc = noalloc_device(&ds, &dev);
+  if (rc != kOk) return rc;
+  KvPlan plan;
+  rc = kvcache_checks(B, H, Sq, Sk, D, ds->sms, &plan);
+  if (rc != kOk) return rc;
+  if (plan.ws_bytes > FATTN_NOALLOC_SCRATCH_BYTES) return FATTN_ERR_TOO_LARGE;
+
+  const size_t bh = (size_t)B * H;
+  const size_t qbytes = bh * Sq * D * 2;
+  const size_t cbytes = bh * Sk * D * 2;
+  const size_t lbytes = bh * Sq * sizeof(float);
+  const size_t nbytes = cache_lens ? (size_t)B * sizeof(int) : 0;
+  const size_t sbytes = status_words ? sizeof(int) * kStatusWords : 0;
+  const void* ins[4] = {q, k_cache, v_cache, cache_lens};
+  const size_t insz[4] = {qbytes, cbytes, cbytes, nbytes};
+  const void* outs[3] = {o, lse, status_words};
+  const size_t outsz[3] = {qbytes, lbytes, sbytes};
+  for (int i = 0; i < 3; ++i) {
+    if (!outsz[i]) continue;
+    for (int j = 0; j < 4; ++j)
+      if (insz[j] && overlaps(outs[i], outsz[i], ins[j], insz[j]))
+        return FATTN_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (outsz[j] && overlaps(outs[i], outsz[i], outs[j], outsz[j]))
+        return FATTN_ERR_INVALID_ARG;
+  }
+  for (int j = 0; j < 4; ++j)
+    if (insz[j] && (rc = check_device_buffer(ins[j], insz[j], dev)) != kOk) return rc;
+  for (int i = 0; i < 3; ++i)
+    if (outsz[i] && (rc = check_device_buffer(outs[i], outsz[i], dev)) != kOk) return rc;
+
+  const bool bf16 = dtype == FATTN_BF16;
+  CUtensorMap tm_k, tm_v;
+  if (encode_cache(&tm_k, k_cache, Sk, (int)bh, D, bf16) != kOk ||
+      encode_cache(&tm_v, v_cache, Sk, (int)bh, D, bf16) != kOk)
+    return FATTN_ERR_CUDA;
+
+  decode::DecodeLaunch a;
+  a.tm_k = &tm_k;
+  a.tm_v = &tm_v;
+  decode::DecodeParams& p = a.params;
+  p.q = q;
+  p.lens = cache_lens;
+  p.part_o = static_cast<float*>(ds->scratch);
+  p.part_lse = static_cast<float*>(ds->scratch) + plan.records * (size_t)Sq * D;
+  p.o = o;
+  p.lse = lse;
+  p.status = status_words ? status_words : ds->status;
+  p.B = B;
+  p.H = H;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.causal = causal != 0;
+  p.n_warps = plan.split_warps;
+  p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  p.timeout_ns = wait_timeout_ns();
+  a.grid = plan.grid;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  if (decode::launch(D, bf16, a) != cudaSuccess) {
+    cudaGetLastError();
+    return FATTN_ERR_LAUNCH;
+  }
+  return FATTN_OK;
 }
 
 }  // extern "C"

@@ -182,6 +182,47 @@ FATTN_API int fattn_kvcache_plan(int B, int H, int Sq, int Sk, int D,
                                  int *grid, int *block, int *smem_bytes,
                                  int *split_warps);
 
+/*
+ * fattn_fwd_kvcache without any device allocation, for callers that cannot
+ * call cudaMalloc.  The pages have no counterpart to this entry point: it is
+ * the same computation as fattn_fwd_kvcache (same kernels, same split, same
+ * results), with the split partials kept in a file-scope static device array
+ * of FATTN_NOALLOC_SCRATCH_BYTES instead of a caller workspace.
+ *
+ * Limit.  The scratch holds (split warps + B*H) * Sq * (D + 1) fp32 values
+ * (fattn_kvcache_plan's workspace_bytes); a call needing more than
+ * FATTN_NOALLOC_SCRATCH_BYTES returns FATTN_ERR_TOO_LARGE before anything is
+ * enqueued.  The scratch needs no clearing: every value the merge kernel
+ * reads is written by the split kernel of the same call.
+ *
+ * First call.  The first call on a device (the current device) queries it
+ * and takes the scratch's address with cudaGetSymbolAddress (its return code
+ * checked; failure gives FATTN_ERR_CUDA); make that first call before any
+ * stream capture begins.  No call allocates device or host memory.
+ *
+ * Concurrency.  Calls on one device share the one scratch array: calls whose
+ * kernels overlap in time (other streams, or other host threads) race on it
+ * and give undefined results.  Calls in order on one stream are safe.
+ *
+ * status_words: device pointer to 4 ints that start at zero (the caller clears
+ * them), or NULL.  Kernel-side errors of this call (a cached length outside
+ * [0, Sk], a pipeline wait past its limit) are recorded there as
+ * fattn_last_error would report them: word 0 the status, word 1 where, word 2
+ * the block or batch index.  With NULL they go to a private static word that
+ * is never read.
+ *
+ * Every other argument, layout and return code as fattn_fwd_kvcache.
+ */
+#define FATTN_NOALLOC_SCRATCH_BYTES (32ull << 20)
+
+FATTN_API int fattn_fwd_kvcache_noalloc(const void *q, const void *k_cache,
+                                        const void *v_cache,
+                                        const int *cache_lens, void *o,
+                                        float *lse, int B, int H, int Sq,
+                                        int Sk, int D, int causal, float scale,
+                                        int dtype, int *status_words,
+                                        fattn_stream_t stream);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 FATTN_API int fattn_version(void);
 
