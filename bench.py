@@ -11,6 +11,12 @@ N > 1 runs under torchrun: every rank runs the same per-GPU workload (weak
 scaling, no collective on the data path); the timing is the max over ranks.
 ``--impl reference`` times the fp64 CPU oracle on a bounded row sample of the
 same workload (the reference arm: this path has no other implementation).
+
+``--kvcache [NAME]`` times attention of new queries against a key/value cache
+instead ("FlashAttention V2", section 6: inference with a KV cache): one step
+is one fattn_fwd_kvcache call on a cache workload of ``attn_inputs`` (default:
+16 sequences, 16 heads, D=128 bf16, one new token, cached lengths 1024..16384),
+reported as effective HBM GB/s against the measured copy bandwidth.
 """
 from __future__ import annotations
 
@@ -460,6 +466,251 @@ def run_sweep(args):
     return 0
 
 
+# ------------------------------------------- attention against a KV cache
+
+KV_METRIC = ("decode attention against a KV cache: effective HBM GB/s "
+             "(cached K/V rows read + Q + O + LSE bytes / time)")
+
+
+def kv_bytes(w, lens) -> int:
+    """Algorithmic bytes of one call: every cached K and V row inside a
+    batch's length read once, Q read, O and the fp32 LSE written once."""
+    rows = int(np.sum(lens)) if lens is not None else w.B * w.Sk
+    return (rows * w.H * w.D * 2 * 2 + 2 * w.B * w.H * w.Sq * w.D * 2
+            + w.B * w.H * w.Sq * 4)
+
+
+def kv_config(w, extra=None) -> dict:
+    lens = (f"cached lengths uniform in [{w.lens_range[0]}, {w.lens_range[1]}] "
+            f"(seed {w.seed})" if w.lens_range else f"every length {w.Sk}")
+    c = {"workload": f"{w.name}: Q/K/V iid N(0,1) seed {w.seed}, {lens}, "
+                     f"{'causal' if w.causal else 'non-causal'}, scale 1/sqrt(D)",
+         "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
+         "l2": "cache larger than L2; no flush"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def kv_oracle_run(x, w, batches: int, seed: int):
+    """The cache oracle on ``batches`` sampled batch entries (all their heads,
+    their cached prefix only); returns (seconds, algorithmic bytes of those
+    entries, threads)."""
+    import oracle
+    threads = oracle.default_threads()
+    rng = np.random.default_rng(seed)
+    pick = rng.choice(w.B, size=min(batches, w.B), replace=False)
+    byts = 0
+    t0 = time.perf_counter()
+    for b in pick.tolist():
+        n = int(x.lens[b]) if x.lens is not None else w.Sk
+        top = max(1, n)
+        oracle.attn_kvcache(x.q[b:b + 1], x.k[b:b + 1, :, :top], x.v[b:b + 1, :, :top],
+                            w.causal, w.scale, [n], threads=threads)
+        byts += w.H * (n * w.D * 2 * 2 + 2 * w.Sq * w.D * 2 + w.Sq * 4)
+    return time.perf_counter() - t0, byts, threads
+
+
+def kv_calibrate(x, w, target_s: float) -> int:
+    """Batch entries per oracle sample so that it takes about ``target_s``
+    (at most every entry)."""
+    n = 1
+    dt, _, _ = kv_oracle_run(x, w, n, 999)
+    while dt < 0.5 and n < w.B:
+        n = min(w.B, n * 4)
+        dt, _, _ = kv_oracle_run(x, w, n, 999)
+    return max(1, min(w.B, int(n * target_s / max(dt, 1e-6))))
+
+
+def kv_cpu_baseline(x, w, target_s: float = 10.0) -> dict:
+    nb = kv_calibrate(x, w, target_s)
+    dt, byts, threads = kv_oracle_run(x, w, nb, 4242)
+    return {"value": byts / dt / 1e9, "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{nb} sampled batch entries (all {w.H} heads) of {w.name} "
+                      f"({dt:.1f} s); algorithmic bytes of those entries / wall time"}
+
+
+def run_kvcache_reference(args, w):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    x = w.inputs()
+    nb = kv_calibrate(x, w, max(0.2, min(10.0, 90.0 / max(1, args.steps + args.warmup))))
+    for i in range(args.warmup):
+        kv_oracle_run(x, w, nb, 100 + i)
+    tot_t, tot_b, threads = 0.0, 0, 1
+    for i in range(args.steps):
+        dt, b, threads = kv_oracle_run(x, w, nb, 1000 + i)
+        tot_t += dt
+        tot_b += b
+    value = tot_b / tot_t / 1e9
+    sample = f"{nb} sampled batch entries (all {w.H} heads) per step of {w.B}"
+    print(json.dumps({
+        "impl": "reference", "metric": KV_METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * tot_t / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": kv_config(w, {"parallelism": "host cores, rank 0 only"}),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+    return 0
+
+
+def load_hbm_peak() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return {"gbs": float(json.load(f)["hbm_gbs"]), "source": "measured"}
+    return {"gbs": 6800.0, "source": "fallback"}
+
+
+def run_kvcache(args, w):
+    """One step = one fattn_fwd_kvcache call (split kernel + merge kernel) on
+    the cache workload, inputs resident in HBM."""
+    import torch
+
+    import exact_attention_forward_10_gb300 as fattn
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+    code = fattn.FATTN_BF16 if w.dtype == "bf16" else fattn.FATTN_FP16
+    x = w.inputs()
+    host = [torch.from_numpy(a).to(tdt).pin_memory() for a in (x.q, x.k, x.v)]
+    h_lens = (torch.from_numpy(x.lens.astype(np.int32)).pin_memory()
+              if x.lens is not None else None)
+    q, k, v = (h.to(dev) for h in host)
+    lens = h_lens.to(dev) if h_lens is not None else None
+    B, H, Sq, Sk, D = w.B, w.H, w.Sq, w.Sk, w.D
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=dev)
+    plan = fattn.fattn_kvcache_plan(B, H, Sq, Sk, D)
+    ws = torch.empty(plan["workspace_bytes"], dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    sptr = stream.cuda_stream
+
+    def launch(qq, kk, vv, ll):
+        rc = fattn.fattn_fwd_kvcache(
+            qq.data_ptr(), kk.data_ptr(), vv.data_ptr(),
+            ll.data_ptr() if ll is not None else 0, o.data_ptr(), lse.data_ptr(),
+            B, H, Sq, Sk, D, w.causal, w.scale, code, ws.data_ptr(), ws.numel(), sptr)
+        if rc != 0:
+            raise fattn.FattnError(rc, "fattn_fwd_kvcache")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    with torch.cuda.stream(stream):
+        launch(q, k, v, lens)
+    rc, where = fattn.fattn_last_error(sptr)
+    if rc != 0:
+        raise RuntimeError(f"kernel status {rc} at {where}")
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            launch(q, k, v, lens)
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.25)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for a, b in ev:
+            a.record(stream)
+            launch(q, k, v, lens)
+            b.record(stream)
+        t1.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    rc, where = fattn.fattn_last_error(sptr)
+    if rc != 0:
+        raise RuntimeError(f"kernel status {rc} at {where}")
+    step_ms = t0.elapsed_time(t1) / args.steps
+    call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    # end to end: the step's inputs (Q, both caches, lengths) copied from
+    # pinned host memory, the call, O and LSE copied back
+    h_o = torch.empty(o.shape, dtype=tdt).pin_memory()
+    h_l = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+
+    def e2e_step():
+        qq, kk, vv = (h.to(dev, non_blocking=True) for h in host)
+        ll = h_lens.to(dev, non_blocking=True) if h_lens is not None else None
+        launch(qq, kk, vv, ll)
+        h_o.copy_(o, non_blocking=True)
+        h_l.copy_(lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    h2d = sum(h.numel() * h.element_size() for h in host) + (
+        h_lens.numel() * 4 if h_lens is not None else 0)
+    d2h = h_o.numel() * h_o.element_size() + h_l.numel() * 4
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([step_ms, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, e2e_ms = float(t[0]), float(t[1])
+    byts = kv_bytes(w, x.lens)
+    value = world * byts / (step_ms * 1e-3) / 1e9
+    peak = load_hbm_peak()
+    achieved = byts / (call_ms * 1e-3) / 1e9
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = kv_cpu_baseline(x, w)
+        print(json.dumps({
+            "metric": KV_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": kv_config(w, {"parallelism": f"replicas x{world}",
+                                    "grid": plan["grid"], "block": plan["block"],
+                                    "split_warps": plan["split_warps"],
+                                    "bytes_per_call": byts}),
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak["gbs"],
+                         "unit": "GB/s", "frac": achieved / peak["gbs"],
+                         "peak_kind": f"HBM copy, {peak['source']}",
+                         "kernel": "fattn_decode_kernel + merge (one call, both "
+                                   "launches inside the timed span)",
+                         "traffic": None},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * byts / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": 2 * args.steps,
+            "clocks": clocks}), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -472,7 +723,18 @@ def main():
     ap.add_argument("--shape", default=None,
                     help="S,D,dtype of a sweep shape (B2 H16) to use as the step "
                          "workload instead of B2 H16 S8192 D128 bf16, e.g. 8192,64,bf16")
+    ap.add_argument("--kvcache", nargs="?", const="decode_b16_h16_d128_ragged",
+                    default=None, choices=sorted(attn_inputs.CACHE_WORKLOADS),
+                    help="time attention of new queries against a KV cache "
+                         "(effective HBM GB/s) on this cache workload")
     args = ap.parse_args()
+    if args.kvcache:
+        if args.warmup < 3:
+            args.warmup = 3
+        w = attn_inputs.CACHE_WORKLOADS[args.kvcache]
+        if args.impl == "reference":
+            return run_kvcache_reference(args, w)
+        return run_kvcache(args, w)
     if args.shape:
         S, D, dt = args.shape.split(",")
         picks = [w for w in attn_inputs.sweep_workloads()

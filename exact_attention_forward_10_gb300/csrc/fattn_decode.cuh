@@ -317,6 +317,10 @@ __global__ void __launch_bounds__(DecodeLayout<D, SQ>::kThreads, 1)
   }
   __syncwarp();
 
+  // The merge grid may start now: it waits for this grid's completion
+  // before it reads a record.
+  asm volatile("griddepcontrol.launch_dependents;");
+
   const int Sq = p.Sq;
   const long long T = total_tiles(p);
   const long long g = (long long)blockIdx.x * L::kWarps + warp;
@@ -543,7 +547,10 @@ __global__ void __launch_bounds__(DecodeLayout<D, SQ>::kThreads, 1)
 //
 // One warp per (head, query row): the head's records are those of the warps
 // whose tile ranges overlap the head's tiles.  Weights 2^(lse_s - max lse);
-// O = sum w_s O_s / sum w_s, LSE = (max lse + log2 sum w_s) * ln 2.
+// O = sum w_s O_s / sum w_s, LSE = (max lse + log2 sum w_s) * ln 2.  It is
+// launched as a programmatic dependent of the split kernel: its set-up
+// overlaps the split kernel's tail, and griddepcontrol.wait orders every
+// record read after the split grid has completed.
 
 constexpr int kCombineWarps = 8;
 
@@ -583,52 +590,72 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kCombineWarps * 32)
     fattn_decode_combine_kernel(const DecodeParams p) {
   constexpr int kCols = D / 32;
+  constexpr int kBatch = 4;  // records loaded together
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
-  if (row >= (long long)p.B * p.H * p.Sq) return;
-  const int bh = (int)(row / p.Sq);
-  const int q = (int)(row % p.Sq);
-  const int b = bh / p.H, h = bh % p.H;
-  long long first;
-  int n;
-  head_tiles(p, b, h, &first, &n);
+  const bool live = row < (long long)p.B * p.H * p.Sq;
+  int bh = 0, q = 0, n = 0;
+  long long first = 0, g0 = 0, g1 = -1, T = 0;
+  const int W = p.n_warps;
+  if (live) {
+    bh = (int)(row / p.Sq);
+    q = (int)(row % p.Sq);
+    head_tiles(p, bh / p.H, bh % p.H, &first, &n);
+    if (n > 0) {
+      T = total_tiles(p);
+      g0 = owner_warp(first, T, W);
+      g1 = owner_warp(first + n - 1, T, W);
+    }
+  }
+  // Everything above only reads the inputs; the records come from the split
+  // kernel, which may still be running when this grid starts early.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (!live) return;
+  // With at least one tile per warp every range is non-empty; otherwise a
+  // warp between the head's first and last owner may hold no tile.
+  const bool dense = T >= W;
+  auto has_record = [&](long long g) {
+    return dense || range_start(g, T, W) < range_start(g + 1, T, W);
+  };
+
+  float M = -INFINITY;
+  for (long long g = g0 + lane; g <= g1; g += 32)
+    if (has_record(g)) M = fmaxf(M, p.part_lse[(g + bh) * p.Sq + q]);
+  M = warp_max(M);
 
   float acc[kCols];
 #pragma unroll
   for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
-  float M = -INFINITY, wsum = 0.f;
-  if (n > 0) {
-    const long long T = total_tiles(p);
-    const int W = p.n_warps;
-    const long long g0 = owner_warp(first, T, W);
-    const long long g1 = owner_warp(first + n - 1, T, W);
-    // pass 1: the largest partial LSE (lanes stride over the records)
-    for (long long g = g0 + lane; g <= g1; g += 32) {
-      if (range_start(g, T, W) < range_start(g + 1, T, W))
-        M = fmaxf(M, p.part_lse[(g + bh) * p.Sq + q]);
-    }
-    M = warp_max(M);
-    // pass 2: weighted sum of the partial outputs
-    if (M != -INFINITY) {
-      for (long long g = g0; g <= g1; ++g) {
-        if (range_start(g, T, W) >= range_start(g + 1, T, W)) continue;
-        const long long rec = (g + bh) * p.Sq + q;
-        const float ls = p.part_lse[rec];
-        if (ls == -INFINITY) continue;
-        const float w = ex2(ls - M);
-        wsum += w;
-        const float* src = p.part_o + rec * D + lane * kCols;
-        if constexpr (kCols == 4) {
-          const float4 v = *reinterpret_cast<const float4*>(src);
-          acc[0] = fmaf(w, v.x, acc[0]);
-          acc[1] = fmaf(w, v.y, acc[1]);
-          acc[2] = fmaf(w, v.z, acc[2]);
-          acc[3] = fmaf(w, v.w, acc[3]);
-        } else {
-          const float2 v = *reinterpret_cast<const float2*>(src);
-          acc[0] = fmaf(w, v.x, acc[0]);
-          acc[1] = fmaf(w, v.y, acc[1]);
+  float wsum = 0.f;
+  if (M != -INFINITY) {
+    for (long long gb = g0; gb <= g1; gb += kBatch) {
+      float ls[kBatch];
+      float v[kBatch][kCols];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const long long g = gb + u;
+        ls[u] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) v[u][c] = 0.f;
+        if (g <= g1 && has_record(g)) {
+          const long long rec = (g + bh) * p.Sq + q;
+          ls[u] = p.part_lse[rec];
+          const float* src = p.part_o + rec * D + lane * kCols;
+          if constexpr (kCols == 4) {
+            const float4 t = *reinterpret_cast<const float4*>(src);
+            v[u][0] = t.x; v[u][1] = t.y; v[u][2] = t.z; v[u][3] = t.w;
+          } else {
+            const float2 t = *reinterpret_cast<const float2*>(src);
+            v[u][0] = t.x; v[u][1] = t.y;
+          }
         }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const float w = ls[u] == -INFINITY ? 0.f : ex2(ls[u] - M);
+        wsum += w;
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) acc[c] = fmaf(w, v[u][c], acc[c]);
       }
     }
   }

@@ -46,11 +46,20 @@ cudaError_t launch_split(const DecodeLaunch& a) {
   kern<<<a.grid, L::kThreads, L::kSmemBytes, a.stream>>>(*a.tm_k, *a.tm_v, a.params);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  // The merge kernel as a programmatic dependent launch: it may begin while
+  // the split kernel finishes and waits (griddepcontrol.wait) for its results.
   const long long rows = (long long)a.params.B * a.params.H * a.params.Sq;
-  const int blocks = (int)((rows + kCombineWarps - 1) / kCombineWarps);
-  fattn_decode_combine_kernel<D, BF16>
-      <<<blocks, kCombineWarps * 32, 0, a.stream>>>(a.params);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((rows + kCombineWarps - 1) / kCombineWarps));
+  cfg.blockDim = dim3(kCombineWarps * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = a.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, &fattn_decode_combine_kernel<D, BF16>, a.params);
 }
 
 template <int D, bool BF16>
