@@ -379,27 +379,37 @@ def run_fattn(args):
     return 0
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources; ties a stored ncu traffic figure to the kernel
-    it was measured on."""
-    import glob
+# The sources each kernel is built from: a stored ncu traffic figure counts
+# only while these files are unchanged.
+KERNEL_SOURCES = {
+    "fattn_fwd": ["fattn_kernel.cuh", "fattn_launch.cuh", "fattn_fwd_d64.cu",
+                  "fattn_fwd_d128.cu", "ptx.cuh", "fattn_status.h"],
+    "fattn_decode": ["fattn_decode.cuh", "fattn_decode_launch.h",
+                     "fattn_decode_d64.cu", "fattn_decode_d128.cu", "ptx.cuh",
+                     "fattn_status.h"],
+}
+
+
+def kernel_source_hash(kernel: str = "fattn_fwd") -> str:
+    """Hash of the CUDA sources of one kernel family; ties a stored ncu
+    traffic figure to the kernel it was measured on."""
     import hashlib
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "exact_attention_forward_10_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "exact_attention_forward_10_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def load_traffic():
-    """DRAM bytes (read + write) per launch of the dominant kernel from the
-    committed ncu summary; None when there is none for the current sources."""
+def load_traffic(key: str = "fattn_fwd_noncausal_bf16_d128", kernel: str = "fattn_fwd"):
+    """DRAM bytes (read + write) per launch of a kernel from the committed ncu
+    summary; None when there is none for the current sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        d = json.load(f).get("fattn_fwd_noncausal_bf16_d128")
-    if not d or d.get("kernel_source_hash") != kernel_source_hash():
+        d = json.load(f).get(key)
+    if not d or d.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
     return d.get("bytes_per_launch")
 
@@ -697,7 +707,8 @@ def run_kvcache(args, w):
                          "peak_kind": f"HBM copy, {peak['source']}",
                          "kernel": "fattn_decode_kernel + merge (one call, both "
                                    "launches inside the timed span)",
-                         "traffic": None},
+                         "traffic": load_traffic(f"fattn_decode_{w.dtype}_d{w.D}_sq{w.Sq}_"
+                                                 f"{args.kvcache}", "fattn_decode")},
             "cpu_baseline": cpu,
             "e2e": {"value": world * byts / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
