@@ -145,14 +145,14 @@ int check_device_buffer(const void* p, size_t bytes, int dev) {
 }
 
 int encode_bhsd(CUtensorMap* tm, const void* ptr, int S, int BH, int D,
-                bool bf16) {
+                bool bf16, int box_rows = kBM) {
   const DriverFns& f = driver();
   if (!f.encode) return kErrCuda;
   // [BH, S, D] viewed as 3-D (D innermost); one box is 64 columns (128 bytes,
-  // the swizzle span) x 128 rows of one head.  Rows past S read as zeros.
+  // the swizzle span) x box_rows rows of one head.  Rows past S read as zeros.
   cuuint64_t gdim[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
   cuuint64_t gstride[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * (cuuint64_t)D * 2};
-  cuuint32_t box[3] = {(cuuint32_t)kSwizzleChunkCols, (cuuint32_t)kBM, 1};
+  cuuint32_t box[3] = {(cuuint32_t)kSwizzleChunkCols, (cuuint32_t)box_rows, 1};
   cuuint32_t estride[3] = {1, 1, 1};
   const CUresult r = f.encode(
       tm, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -214,10 +214,16 @@ struct Plan {
 
 int host_checks(int B, int H, int S, int D, Plan* plan) {
   if (B < 1 || H < 1 || S < 1) return kErrInvalidArg;
-  if (D != 64 && D != 128) return kErrUnsupported;
+  if (D != 64 && D != 128 && D != 256) return kErrUnsupported;
   const long long rows = (long long)B * H * S;
   if (rows > INT_MAX) return kErrTooLarge;
-  if (D == 64) {
+  if (D == 256) {
+    // the CTA-pair kernel: a unit is 256 query rows, one 128-row tile per SM
+    plan->qt = 2;
+    plan->ns = kPairStages;
+    plan->threads = PairShape::kThreads;
+    plan->smem = PairShape::kSmem;
+  } else if (D == 64) {
     plan->qt = FwdConfig<64>::QT;
     plan->ns = FwdConfig<64>::NS;
     plan->threads = FwdShape<64>::kThreads;
@@ -292,6 +298,28 @@ int noalloc_device(NoAllocState** out, int* dev_out) {
   return kOk;
 }
 
+// CTAs of the persistent grid: one per SM, but for the CTA-pair kernel (D =
+// 256) twice the clusters that fit at once (occupancy query, cached per
+// device and mask/dtype).
+int fwd_grid(const Plan& plan, int D, bool causal, bool bf16, int sms) {
+  if (D != 256) return plan.total_units < sms ? plan.total_units : sms;
+  static int fit[kMaxDevices][4] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  int* slot = dev < kMaxDevices ? &fit[dev][(causal ? 2 : 0) + (bf16 ? 1 : 0)] : nullptr;
+  int clusters = slot ? *slot : 0;
+  if (clusters <= 0) {
+    clusters = pair_clusters_d256(causal, bf16);
+    if (slot) *slot = clusters;
+  }
+  if (clusters <= 0) return 0;
+  if (plan.total_units < clusters) clusters = plan.total_units;
+  return 2 * clusters;
+}
+
 }  // namespace
 }  // namespace fattn
 
@@ -322,9 +350,12 @@ FATTN_API int fattn_plan(int B, int H, int S, int D, int causal, int* grid,
   Plan plan;
   const int rc = host_checks(B, H, S, D, &plan);
   if (rc != kOk) return rc;
-  int g = plan.total_units;
+  int g = D == 256 ? 2 * plan.total_units : plan.total_units;
   DeviceState* ds = nullptr;
-  if (current_device(&ds, nullptr) == kOk && ds->sms < g) g = ds->sms;
+  if (current_device(&ds, nullptr) == kOk) {
+    const int fg = fwd_grid(plan, D, causal != 0, true, ds->sms);
+    if (fg > 0) g = fg;
+  }
   if (grid) *grid = g;
   if (block) *block = plan.threads;
   if (smem_bytes) *smem_bytes = plan.smem;
@@ -371,8 +402,9 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o,
   const bool bf16 = dtype == FATTN_BF16;
   const int BH = B * H;
   CUtensorMap tm_q, tm_k, tm_v;
+  // the CTA-pair kernel loads K in halves of 64 keys
   if (encode_bhsd(&tm_q, q, S, BH, D, bf16) != kOk ||
-      encode_bhsd(&tm_k, k, S, BH, D, bf16) != kOk ||
+      encode_bhsd(&tm_k, k, S, BH, D, bf16, D == 256 ? 64 : kBM) != kOk ||
       encode_bhsd(&tm_v, v, S, BH, D, bf16) != kOk)
     return FATTN_ERR_CUDA;
 
@@ -390,11 +422,13 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o,
   a.params.total_units = plan.total_units;
   a.params.scale_log2 = (float)((double)scale * 1.4426950408889634);
   a.params.timeout_ns = wait_timeout_ns();
-  a.grid = plan.total_units < ds->sms ? plan.total_units : ds->sms;
+  a.grid = fwd_grid(plan, D, causal != 0, bf16, ds->sms);
+  if (a.grid <= 0) return FATTN_ERR_LAUNCH;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
 
-  const cudaError_t e = D == 64 ? launch_fwd_d64(causal != 0, bf16, a)
-                                : launch_fwd_d128(causal != 0, bf16, a);
+  const cudaError_t e = D == 64    ? launch_fwd_d64(causal != 0, bf16, a)
+                        : D == 128 ? launch_fwd_d128(causal != 0, bf16, a)
+                                   : launch_fwd_d256(causal != 0, bf16, a);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return FATTN_ERR_LAUNCH;

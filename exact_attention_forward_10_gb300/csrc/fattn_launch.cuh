@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 
 #include "fattn_kernel.cuh"
+#include "fattn_kernel_pair.cuh"
 
 namespace fattn {
 
@@ -65,8 +66,70 @@ cudaError_t launch_fwd(const LaunchArgs& a) {
   return cudaGetLastError();
 }
 
+// Head dim 256: the CTA-pair kernel (clusters of two CTAs, one per SM).
+constexpr int kPairStages = 5;
+struct PairShape {
+  static constexpr int kSmem = pair::PairLayout<kPairStages>::kSmemBytes;
+  static constexpr int kThreads = pair::PairWarps::kThreads;
+};
+
+template <bool CAUSAL, bool BF16>
+cudaError_t set_pair_attr() {
+  auto kern = &pair::fattn_fwd_pair_kernel<kPairStages, CAUSAL, BF16>;
+  static volatile bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PairShape::kSmem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set[dev] = true;
+  }
+  return cudaSuccess;
+}
+
+// a.grid counts CTAs (twice the clusters).
+template <bool CAUSAL, bool BF16>
+cudaError_t launch_fwd_pair(const LaunchArgs& a) {
+  cudaError_t e = set_pair_attr<CAUSAL, BF16>();
+  if (e != cudaSuccess) return e;
+  pair::fattn_fwd_pair_kernel<kPairStages, CAUSAL, BF16>
+      <<<a.grid, PairShape::kThreads, PairShape::kSmem, a.stream>>>(*a.tm_q, *a.tm_k,
+                                                                     *a.tm_v, a.params);
+  return cudaGetLastError();
+}
+
+// Clusters of the pair kernel that fit on the current device at once (the
+// persistent grid must not exceed it: work is assigned to clusters
+// statically).  0 on error.
+template <bool CAUSAL, bool BF16>
+int pair_clusters_fit() {
+  if (set_pair_attr<CAUSAL, BF16>() != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(PairShape::kThreads);
+  cfg.dynamicSmemBytes = PairShape::kSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, &pair::fattn_fwd_pair_kernel<kPairStages, CAUSAL, BF16>,
+                                     &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 // Defined in the instantiation units.
 cudaError_t launch_fwd_d64(bool causal, bool bf16, const LaunchArgs& a);
 cudaError_t launch_fwd_d128(bool causal, bool bf16, const LaunchArgs& a);
+cudaError_t launch_fwd_d256(bool causal, bool bf16, const LaunchArgs& a);
+int pair_clusters_d256(bool causal, bool bf16);
 
 }  // namespace fattn

@@ -52,7 +52,8 @@ enum fattn_status {
   FATTN_ERR_INVALID_ARG = -1,      /* null pointer, B/H/S < 1, bad scale,
                                       overlapping buffers, non-device memory
                                       or a buffer smaller than its tensor */
-  FATTN_ERR_UNSUPPORTED = -2,      /* D not in {64, 128}, unknown dtype, no
+  FATTN_ERR_UNSUPPORTED = -2,      /* D not in {64, 128, 256} (the cache
+                                      entry points: {64, 128}), unknown dtype, no
                                       CUDA device, device is not sm_103, or
                                       (cache attention) Sq > 16 */
   FATTN_ERR_MISALIGNED = -3,       /* q/k/v/o not 16-byte aligned, lse not
@@ -73,7 +74,7 @@ enum fattn_dtype { FATTN_FP16 = 0, FATTN_BF16 = 1 };
  *   o        device pointer to the output, 16-byte aligned
  *   lse      device pointer to the fp32 log-sum-exp output, 4-byte aligned
  *   B, H, S  batch, heads, sequence length (each >= 1)
- *   D        head dimension: 64 or 128
+ *   D        head dimension: 64, 128 or 256 (256 runs on pairs of SMs)
  *   causal   0: every key; non-zero: key index <= query index
  *   scale    score multiplier, finite and > 0 (usually 1/sqrt(D))
  *   dtype    FATTN_FP16 or FATTN_BF16 (inputs and output)
@@ -104,10 +105,12 @@ FATTN_API const char *fattn_error_string(int status);
  * The launch fattn_fwd would make for these sizes, without launching.
  * Fills (each pointer may be NULL): grid (CTAs), block (threads), dynamic
  * shared memory bytes, work units (query-tile groups over all heads), query
- * tiles of 128 rows per unit, and K/V pipeline stages.  Needs a device only
- * for the grid (it depends on the SM count); without one *grid is set to the
- * number of units.  Returns FATTN_OK or the status fattn_fwd would return
- * for the same sizes' host-side checks.
+ * tiles of 128 rows per unit, and K/V pipeline stages.  For D = 256 a unit is
+ * served by a cluster of two CTAs (one query tile each) and the grid counts
+ * CTAs.  Needs a device only for the grid (it depends on the SM count and,
+ * for D = 256, on how many clusters fit); without one *grid is set to the
+ * number of CTAs the units would use.  Returns FATTN_OK or the status
+ * fattn_fwd would return for the same sizes' host-side checks.
  */
 FATTN_API int fattn_plan(int B, int H, int S, int D, int causal, int *grid,
                          int *block, int *smem_bytes, int *units,

@@ -61,7 +61,7 @@ P = 1 << 20
     (dict(scale=float("nan")), fattn.FATTN_ERR_INVALID_ARG),
     (dict(scale=float("inf")), fattn.FATTN_ERR_INVALID_ARG),
     (dict(D=96), fattn.FATTN_ERR_UNSUPPORTED),
-    (dict(D=256), fattn.FATTN_ERR_UNSUPPORTED),
+    (dict(D=512), fattn.FATTN_ERR_UNSUPPORTED),
     (dict(dtype=2), fattn.FATTN_ERR_UNSUPPORTED),
     (dict(q=P + 8), fattn.FATTN_ERR_MISALIGNED),
     (dict(o=P * 9 + 2), fattn.FATTN_ERR_MISALIGNED),
@@ -89,6 +89,13 @@ def test_plan_without_device(lib):
     assert 1 <= p["grid"] <= p["units"]
     with pytest.raises(fattn.FattnError):
         fattn.fattn_plan(1, 1, 10, 80)
+
+
+def test_plan_head_dim_256_uses_cta_pairs(lib):
+    p = fattn.fattn_plan(2, 16, 8192, 256, False)
+    assert p["q_tiles_per_unit"] == 2 and p["units"] == 2 * 16 * (8192 // 256)
+    assert p["smem_bytes"] <= 232448 and p["block"] == 384
+    assert p["grid"] % 2 == 0 and 2 <= p["grid"] <= 2 * p["units"]
 
 
 @pytest.mark.parametrize("args,want", [
