@@ -342,7 +342,8 @@ def run_fattn(args):
     # dominant kernel: the non-causal launch (2/3 of the step's FLOPs)
     dom_ms = statistics.mean(per_launch[False])
     achieved = metric_flops(B, H, S, D, False) / (dom_ms * 1e-3) / 1e12
-    traffic = load_traffic()
+    traffic = load_traffic(f"fattn_fwd_noncausal_{w.dtype}_d{D}_s{S}",
+                           "fattn_pair" if D == 256 else "fattn_fwd")
     plan = fattn.fattn_plan(B, H, S, D, False)
 
     result = None
@@ -363,7 +364,9 @@ def run_fattn(args):
                          "peak": peaks["burst"], "unit": "TFLOP/s",
                          "frac": achieved / peaks["burst"],
                          "peak_kind": f"bf16 dense, {peaks['source']} burst",
-                         "kernel": "fattn_fwd_kernel<D=128, non-causal, bf16>",
+                         "kernel": (f"fattn_fwd_pair_kernel<D=256, non-causal, {w.dtype}> "
+                                    "(CTA pairs)" if w.D == 256 else
+                                    f"fattn_fwd_kernel<D={w.D}, non-causal, {w.dtype}>"),
                          "traffic": traffic},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -384,6 +387,8 @@ def run_fattn(args):
 KERNEL_SOURCES = {
     "fattn_fwd": ["fattn_kernel.cuh", "fattn_launch.cuh", "fattn_fwd_d64.cu",
                   "fattn_fwd_d128.cu", "ptx.cuh", "fattn_status.h"],
+    "fattn_pair": ["fattn_kernel_pair.cuh", "fattn_kernel.cuh", "fattn_launch.cuh",
+                   "fattn_fwd_d256.cu", "ptx.cuh", "fattn_status.h"],
     "fattn_decode": ["fattn_decode.cuh", "fattn_decode_launch.h",
                      "fattn_decode_d64.cu", "fattn_decode_d128.cu", "ptx.cuh",
                      "fattn_status.h"],
@@ -435,7 +440,13 @@ def run_sweep(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     peaks = load_peaks()
     stream = torch.cuda.Stream(dev)
-    for w in attn_inputs.sweep_workloads():
+    dims = [int(d) for d in args.dims.split(",")]
+    shapes = [w for w in attn_inputs.sweep_workloads() if w.D in dims]
+    if 256 in dims:
+        shapes += [attn_inputs.Workload(f"B2_H16_S{S}_D256_{dt}", 2, 16, S, 256, dt,
+                                        (False, True), 100)
+                   for S in attn_inputs.SWEEP_S for dt in attn_inputs.DTYPES]
+    for w in shapes:
         tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
         code = fattn.FATTN_BF16 if w.dtype == "bf16" else fattn.FATTN_FP16
         g = torch.Generator(device=dev)
@@ -732,8 +743,12 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="TFLOPS over the sweep shapes, one JSON line each")
     ap.add_argument("--shape", default=None,
-                    help="S,D,dtype of a sweep shape (B2 H16) to use as the step "
-                         "workload instead of B2 H16 S8192 D128 bf16, e.g. 8192,64,bf16")
+                    help="S,D,dtype (B2 H16) to use as the step workload instead of "
+                         "B2 H16 S8192 D128 bf16, e.g. 8192,64,bf16 or 8192,256,bf16 "
+                         "(sweep shapes keep their seeds; others use seed 100)")
+    ap.add_argument("--dims", default="64,128",
+                    help="head dims of --sweep (64,128 are the sweep's; 256 adds the "
+                         "CTA-pair kernel)")
     ap.add_argument("--kvcache", nargs="?", const="decode_b16_h16_d128_ragged",
                     default=None, choices=sorted(attn_inputs.CACHE_WORKLOADS),
                     help="time attention of new queries against a KV cache "
@@ -751,7 +766,11 @@ def main():
         picks = [w for w in attn_inputs.sweep_workloads()
                  if (w.S, w.D, w.dtype) == (int(S), int(D), dt)]
         if not picks:
-            ap.error(f"no sweep shape {args.shape}")
+            if dt not in attn_inputs.DTYPES or int(D) not in (64, 128, 256):
+                ap.error(f"bad shape {args.shape}")
+            # a shape outside the sweep (e.g. head dim 256): B2 H16, seed 100
+            picks = [attn_inputs.Workload(f"B2_H16_S{S}_D{D}_{dt}", 2, 16, int(S), int(D),
+                                          dt, (False, True), 100)]
         global WORKLOAD
         WORKLOAD = picks[0]
     if args.warmup < 3:
