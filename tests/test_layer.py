@@ -1,0 +1,141 @@
+"""The attention layer built on the kernel ("FlashAttention-2 in an attention
+layer"): the same layer computed with a plain fp32 PyTorch attention that
+materialises the T x T scores agrees with it; its peak memory grows about
+linearly in T while the materialising layer's grows about quadratically; the
+attention call allocates nothing of size T x T; and it is faster than the
+materialising layer.  Weights and inputs are random (seeded)."""
+import math
+
+import pytest
+import torch
+
+from exact_attention_forward_10_gb300 import layer as L
+
+
+def test_state_is_far_smaller_than_the_score_matrix():
+    """Shape algebra (CPU): at B=1, H=32, T=2048, D=128 in 16-bit the T x T
+    scores alone are 256 MiB; the fused call adds O and the LSE only."""
+    naive = L.score_matrix_bytes(1, 32, 2048)
+    state = L.attention_state_bytes(1, 32, 2048, 128)
+    assert naive == 256 * 2**20
+    assert state == 32 * 2048 * (128 * 2 + 4)
+    assert state < naive / 15
+    # the gap widens linearly with T
+    assert (L.score_matrix_bytes(1, 32, 8192) / L.attention_state_bytes(1, 32, 8192, 128)
+            == pytest.approx(4 * naive / state))
+
+
+def test_layer_rejects_bad_shapes():
+    with pytest.raises(ValueError):
+        L.ExactAttention(1000, 16)     # not a multiple
+    with pytest.raises(ValueError):
+        L.ExactAttention(96 * 4, 4)    # head dim 96
+
+
+def _materialising_attention(layer, x):
+    """The same layer with attention computed in fp32 by plain PyTorch ops,
+    T x T scores materialised (the quadratic-memory way)."""
+    q, k, v = (t.float() for t in layer.split_heads(x))
+    s = (q @ k.transpose(-1, -2)) / math.sqrt(layer.head_dim)
+    T = s.shape[-1]
+    if layer.causal:
+        mask = torch.ones(T, T, dtype=torch.bool, device=s.device).tril()
+        s = s.masked_fill(~mask, float("-inf"))
+    o = torch.softmax(s, dim=-1) @ v
+    return layer.merge_heads(o.to(x.dtype))
+
+
+@pytest.fixture(scope="module")
+def cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("d_model,heads,dtype", [(1024, 16, torch.float16),
+                                                 (1024, 8, torch.bfloat16),
+                                                 (2048, 8, torch.float16)])
+def test_layer_matches_materialising_layer(cuda, d_model, heads, dtype):
+    torch.manual_seed(0)
+    layer = L.ExactAttention(d_model, heads, device=cuda, dtype=dtype)
+    x = torch.randn(2, 300, d_model, device=cuda, dtype=dtype)
+    with torch.inference_mode():
+        y, lse = layer(x, return_lse=True)
+        y_ref = _materialising_attention(layer, x)
+    torch.cuda.synchronize()
+    err = (y.float() - y_ref.float()).abs().max().item()
+    # both outputs go through the same 16-bit output projection; the
+    # attention outputs differ by at most the kernel tolerance
+    tol = 2e-3 if dtype == torch.float16 else 1.5e-2
+    scale = layer.out.weight.float().abs().sum(dim=1).max().item()
+    assert err <= tol * scale, f"max |dy| = {err:.3e} (bound {tol * scale:.3e})"
+    assert torch.isfinite(lse).all() and lse.shape == (2, heads, 300)
+
+
+def _peak_bytes(fn):
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    with torch.inference_mode():
+        fn()
+    torch.cuda.synchronize()
+    return torch.cuda.max_memory_allocated() - base
+
+
+@pytest.mark.gpu
+def test_memory_grows_linearly_in_T(cuda):
+    """T from 512 to 2048 (4x): the kernel layer's peak grows at most about
+    4x (linear); the materialising layer's grows far more (quadratic)."""
+    torch.manual_seed(0)
+    layer = L.ExactAttention(1024, 16, device=cuda, dtype=torch.float16)
+    peaks = {}
+    for T in (512, 2048):
+        x = torch.randn(1, T, 1024, device=cuda, dtype=torch.float16)
+        peaks[("fused", T)] = _peak_bytes(lambda: layer(x))
+        peaks[("naive", T)] = _peak_bytes(lambda: _materialising_attention(layer, x))
+    fused = peaks[("fused", 2048)] / peaks[("fused", 512)]
+    naive = peaks[("naive", 2048)] / peaks[("naive", 512)]
+    assert fused <= 5.0, f"kernel layer peak grew {fused:.1f}x for 4x T"
+    assert naive >= 8.0, f"materialising layer grew only {naive:.1f}x"
+    assert peaks[("fused", 2048)] < peaks[("naive", 2048)] / 4
+
+
+@pytest.mark.gpu
+def test_attention_call_allocates_no_score_matrix(cuda):
+    """The attention call itself adds O and the LSE and nothing more."""
+    import exact_attention_forward_10_gb300 as fattn
+    B, H, T, D = 1, 32, 2048, 128
+    q, k, v = (torch.randn(B, H, T, D, device=cuda, dtype=torch.float16) for _ in range(3))
+    fattn.forward(q, k, v, causal=True)  # first call: library set-up
+    extra = _peak_bytes(lambda: fattn.forward(q, k, v, causal=True))
+    assert extra <= L.attention_state_bytes(B, H, T, D) + (1 << 20)
+    assert extra < L.score_matrix_bytes(B, H, T) / 16
+
+
+@pytest.mark.gpu
+def test_layer_is_faster_than_materialising_layer(cuda):
+    torch.manual_seed(0)
+    layer = L.ExactAttention(4096, 32, device=cuda, dtype=torch.float16)
+    x = torch.randn(1, 2048, 4096, device=cuda, dtype=torch.float16)
+
+    def timed(fn, n=10):
+        with torch.inference_mode():
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(n):
+                fn()
+            b.record()
+            b.synchronize()
+        return a.elapsed_time(b) / n
+
+    t_fused = timed(lambda: layer(x))
+    t_naive = timed(lambda: _materialising_attention(layer, x))
+    print(f"layer B1 T2048 d4096 H32: fused {t_fused:.3f} ms, materialising {t_naive:.3f} ms")
+    assert t_fused * 1.5 < t_naive
