@@ -113,7 +113,8 @@ def test_attention_call_allocates_no_score_matrix(cuda):
     fattn.forward(q, k, v, causal=True)  # first call: library set-up
     extra = _peak_bytes(lambda: fattn.forward(q, k, v, causal=True))
     assert extra <= L.attention_state_bytes(B, H, T, D) + (1 << 20)
-    assert extra < L.score_matrix_bytes(B, H, T) / 16
+    # O alone is T/D = 16 times smaller than the scores here; nothing else
+    assert extra * 8 < L.score_matrix_bytes(B, H, T)
 
 
 @pytest.mark.gpu
