@@ -284,3 +284,87 @@ CACHE_WORKLOADS = {
         "decode_B8_H16_Sq4_Sk8192_D64_fp16_causal_lens1-8192", 8, 16, 4, 8192,
         64, "fp16", True, 42, (1, 8192)),
 }
+
+
+# --------------------------------------------------------------------------
+# 8-bit inputs: OCP FP8 E4M3 (the "fn" variant: bias 7, three mantissa bits,
+# no infinities, largest finite value 448, subnormals m/8 * 2^-6), for the
+# FP8 forward ("FlashAttention V2", section 7: FP8 attention).  Each tensor
+# carries one fp32 dequantisation scale: real value = code value * scale.
+# --------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    """Values of E4M3 codes (uint8) as float64; the NaN codes 0x7F, 0xFF
+    decode to NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 15
+    m = c & 7
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    val = np.where((c & 0x7F) == 0x7F, np.nan, val)
+    return sign * val
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """Round finite values to E4M3 codes: nearest, ties to even mantissa,
+    magnitudes above 448 saturate to 448 (the finite-saturating cast)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    # exponent of the binade, at least the subnormal one (2^-6)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)
+    quantum = np.exp2(e - 3.0)
+    q = np.round(a / quantum) * quantum        # numpy rounds half to even
+    q = np.minimum(q, E4M3_MAX)
+    q = np.where(a == 0, 0.0, q)
+    # encode q (exactly representable now)
+    eq = np.floor(np.log2(np.where(q > 0, q, 1.0)))
+    sub = q < 2.0 ** -6
+    mant_sub = np.round(q / 2.0 ** -9).astype(np.int64)              # m/8 * 2^-6
+    exp_n = (eq + 7).astype(np.int64)
+    mant_n = np.round((q / np.exp2(eq) - 1.0) * 8.0).astype(np.int64)
+    code = np.where(sub, mant_sub, (exp_n << 3) | mant_n)
+    code = np.where(q == 0, 0, code)
+    return (code | np.where(x < 0, 0x80, 0)).astype(np.uint8)
+
+
+@dataclasses.dataclass
+class QKV8:
+    """E4M3 inputs: ``q8, k8, v8`` uint8 codes [B, H, S, D]; ``descale`` the
+    three per-tensor scales; ``q, k, v`` the real values (code value times
+    scale, exact in float64)."""
+
+    q8: np.ndarray
+    k8: np.ndarray
+    v8: np.ndarray
+    descale: tuple
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    seed: int
+
+
+def make_qkv_fp8(B: int, H: int, S: int, D: int, seed: int,
+                 qk_mult: float = 1.0) -> QKV8:
+    """Q, K, V i.i.d. N(0,1) from ``seed`` (the same stream and order as
+    ``make_qkv``), each multiplied by ``qk_mult`` (Q and K only), then
+    quantised per tensor: scale = a power of two putting the tensor's largest
+    magnitude at or below 448, code = E4M3 rounding of value / scale."""
+    n = B * H * S * D
+    shape = (B, H, S, D)
+    out = []
+    for i, mult in enumerate((qk_mult, qk_mult, 1.0)):
+        x = np.empty(n, dtype=np.float64)
+        for c0 in range(0, n, _CHUNK):
+            c1 = min(n, c0 + _CHUNK)
+            x[c0:c1] = normals(seed, i * n + c0, c1 - c0)
+        x *= mult
+        amax = float(np.abs(x).max()) if n else 1.0
+        scale = 2.0 ** math.ceil(math.log2(amax / E4M3_MAX)) if amax > 0 else 1.0
+        codes = e4m3_encode(x / scale).reshape(shape)
+        out.append((codes, scale, e4m3_decode(codes) * scale))
+    (q8, qs, q), (k8, ks, k), (v8, vs, v) = out
+    return QKV8(q8=q8, k8=k8, v8=v8, descale=(qs, ks, vs), q=q, k=k, v=v, seed=seed)

@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
         l.fattn_kvcache_plan.argtypes = [i, i, i, i, i, ctypes.POINTER(u64),
                                          ip, ip, ip, ip]
         l.fattn_kvcache_plan.restype = i
+        l.fattn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, f, f, f, i, vp]
+        l.fattn_fwd_fp8.restype = i
         l.fattn_fwd_kvcache_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i,
                                                 i, i, i, i, f, i, vp, vp]
         l.fattn_fwd_kvcache_noalloc.restype = i
@@ -106,6 +108,14 @@ def fattn_plan(B, H, S, D, causal=False) -> dict:
     keys = ("grid", "block", "smem_bytes", "units", "q_tiles_per_unit",
             "kv_stages")
     return {k_: x.value for k_, x in zip(keys, vals)}
+
+
+def fattn_fwd_fp8(q, k, v, o, lse, B, H, S, D, causal, scale, q_scale, k_scale,
+                  v_scale, out_dtype, stream) -> int:
+    """``fattn_fwd_fp8`` with integer device pointers and an integer stream."""
+    return lib().fattn_fwd_fp8(q, k, v, o, lse, B, H, S, D, int(causal), float(scale),
+                               float(q_scale), float(k_scale), float(v_scale),
+                               out_dtype, stream)
 
 
 def fattn_fwd_kvcache(q, k_cache, v_cache, cache_lens, o, lse, B, H, Sq, Sk,
@@ -238,4 +248,37 @@ def forward_kvcache(q, k_cache, v_cache, cache_lens=None, causal: bool = False,
                            stream.cuda_stream)
     if rc != FATTN_OK:
         raise FattnError(rc, "fattn_fwd_kvcache")
+    return out, lse
+
+
+def forward_fp8(q8, k8, v8, q_scale: float, k_scale: float, v_scale: float,
+                causal: bool = False, scale: float | None = None, out_dtype=None,
+                out=None, lse=None, stream=None):
+    """Attention with E4M3 inputs.  ``q8, k8, v8``: contiguous ``[B, H, S,
+    128]`` CUDA tensors of E4M3 codes (``torch.uint8`` or
+    ``torch.float8_e4m3fn``); real values are code value times the scale.
+    Returns ``(o, lse)``; ``o`` in ``out_dtype`` (default bf16)."""
+    import torch
+    if q8.dim() != 4 or q8.shape != k8.shape or q8.shape != v8.shape:
+        raise ValueError("q8, k8, v8 must share one [B, H, S, D] shape")
+    for t in (q8, k8, v8):
+        if t.element_size() != 1 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q8, k8, v8 must be contiguous one-byte CUDA tensors")
+    B, H, S, D = q8.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out_dtype is None:
+        out_dtype = torch.bfloat16
+    code = _dtype_code(torch.empty(0, dtype=out_dtype))
+    if out is None:
+        out = torch.empty((B, H, S, D), dtype=out_dtype, device=q8.device)
+    if lse is None:
+        lse = torch.empty((B, H, S), dtype=torch.float32, device=q8.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q8.device)
+    rc = fattn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(),
+                       lse.data_ptr(), B, H, S, D, causal, scale, q_scale, k_scale,
+                       v_scale, code, stream.cuda_stream)
+    if rc != FATTN_OK:
+        raise FattnError(rc, "fattn_fwd_fp8")
     return out, lse

@@ -25,6 +25,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libfattn.so")
 
 SOURCES = ["fattn_api.cu", "fattn_fwd_d64.cu", "fattn_fwd_d128.cu", "fattn_fwd_d256.cu",
+           "fattn_fwd_fp8.cu",
            "fattn_decode.cu", "fattn_decode_d64.cu", "fattn_decode_d128.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -144,6 +144,21 @@ int check_device_buffer(const void* p, size_t bytes, int dev) {
   return kOk;
 }
 
+// The same for E4M3 inputs: one box is 128 columns (128 bytes) x 128 rows.
+int encode_bhsd_e4m3(CUtensorMap* tm, const void* ptr, int S, int BH, int D) {
+  const DriverFns& f = driver();
+  if (!f.encode) return kErrCuda;
+  cuuint64_t gdim[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)BH};
+  cuuint64_t gstride[2] = {(cuuint64_t)D, (cuuint64_t)S * (cuuint64_t)D};
+  cuuint32_t box[3] = {128, (cuuint32_t)kBM, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  const CUresult r = f.encode(
+      tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), gdim, gstride, box,
+      estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? kOk : kErrCuda;
+}
+
 int encode_bhsd(CUtensorMap* tm, const void* ptr, int S, int BH, int D,
                 bool bf16, int box_rows = kBM) {
   const DriverFns& f = driver();
@@ -421,6 +436,7 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o,
   a.params.n_units = plan.units_per_head;
   a.params.total_units = plan.total_units;
   a.params.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  a.params.o_scale = 1.0f;
   a.params.timeout_ns = wait_timeout_ns();
   a.grid = fwd_grid(plan, D, causal != 0, bf16, ds->sms);
   if (a.grid <= 0) return FATTN_ERR_LAUNCH;
@@ -536,6 +552,78 @@ FATTN_API int fattn_fwd_kvcache(const void* q, const void* k_cache,
   a.grid = plan.grid;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   if (decode::launch(D, bf16, a) != cudaSuccess) {
+    cudaGetLastError();
+    return FATTN_ERR_LAUNCH;
+  }
+  return FATTN_OK;
+}
+
+FATTN_API int fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o,
+                            float* lse, int B, int H, int S, int D, int causal,
+                            float scale, float q_scale, float k_scale, float v_scale,
+                            int out_dtype, fattn_stream_t stream) {
+  // ---- host-side checks, nothing enqueued yet
+  if (!q || !k || !v || !o || !lse) return FATTN_ERR_INVALID_ARG;
+  for (float x : {scale, q_scale, k_scale, v_scale})
+    if (!(x > 0.0f) || !std::isfinite(x)) return FATTN_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || S < 1) return FATTN_ERR_INVALID_ARG;
+  if (D != 128) return FATTN_ERR_UNSUPPORTED;
+  if (out_dtype != FATTN_FP16 && out_dtype != FATTN_BF16) return FATTN_ERR_UNSUPPORTED;
+  const long long rows = (long long)B * H * S;
+  if (rows > INT_MAX) return FATTN_ERR_TOO_LARGE;
+  const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  if ((a16 & 15u) != 0 || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return FATTN_ERR_MISALIGNED;
+  const size_t ibytes = (size_t)rows * D;      // E4M3
+  const size_t obytes = (size_t)rows * D * 2;  // 16-bit output
+  const size_t lbytes = (size_t)rows * sizeof(float);
+  if (overlaps(o, obytes, q, ibytes) || overlaps(o, obytes, k, ibytes) ||
+      overlaps(o, obytes, v, ibytes) || overlaps(lse, lbytes, q, ibytes) ||
+      overlaps(lse, lbytes, k, ibytes) || overlaps(lse, lbytes, v, ibytes) ||
+      overlaps(lse, lbytes, o, obytes))
+    return FATTN_ERR_INVALID_ARG;
+
+  DeviceState* ds = nullptr;
+  int dev = 0;
+  int rc = current_device(&ds, &dev);
+  if (rc != kOk) return rc;
+  if ((rc = check_device_buffer(q, ibytes, dev)) != kOk) return rc;
+  if ((rc = check_device_buffer(k, ibytes, dev)) != kOk) return rc;
+  if ((rc = check_device_buffer(v, ibytes, dev)) != kOk) return rc;
+  if ((rc = check_device_buffer(o, obytes, dev)) != kOk) return rc;
+  if ((rc = check_device_buffer(lse, lbytes, dev)) != kOk) return rc;
+
+  const int BH = B * H;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (encode_bhsd_e4m3(&tm_q, q, S, BH, D) != kOk ||
+      encode_bhsd_e4m3(&tm_k, k, S, BH, D) != kOk ||
+      encode_bhsd_e4m3(&tm_v, v, S, BH, D) != kOk)
+    return FATTN_ERR_CUDA;
+  const int units_per_head = (S + 2 * kBM - 1) / (2 * kBM);
+  const long long total = (long long)BH * units_per_head;
+  if (total > INT_MAX) return FATTN_ERR_TOO_LARGE;
+
+  LaunchArgs a;
+  a.tm_q = &tm_q;
+  a.tm_k = &tm_k;
+  a.tm_v = &tm_v;
+  a.params.o = o;
+  a.params.lse = lse;
+  a.params.status = ds->status;
+  a.params.S = S;
+  a.params.BH = BH;
+  a.params.n_kv_tiles = (S + kBN - 1) / kBN;
+  a.params.n_units = units_per_head;
+  a.params.total_units = (int)total;
+  // scores of the real values: scale * (q_scale Q8) . (k_scale K8)
+  a.params.scale_log2 =
+      (float)((double)scale * q_scale * k_scale * 1.4426950408889634);
+  a.params.o_scale = v_scale;
+  a.params.timeout_ns = wait_timeout_ns();
+  a.grid = (int)total < ds->sms ? (int)total : ds->sms;
+  a.stream = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_fwd_fp8_d128(causal != 0, out_dtype == FATTN_BF16, a) != cudaSuccess) {
     cudaGetLastError();
     return FATTN_ERR_LAUNCH;
   }

@@ -76,14 +76,21 @@ struct FwdParams {
   int n_kv_tiles;     // ceil(S / kBN)
   int n_units;        // work units per head: ceil(S / (kBM * QT))
   int total_units;    // BH * n_units
-  float scale_log2;   // scale * log2(e)
+  float scale_log2;   // scale * log2(e) (FP8: times the Q and K scales)
+  float o_scale;      // multiplies O in the epilogue (FP8: the V scale; else 1)
   unsigned long long timeout_ns;
 };
 
-template <int D, int QT, int NS>
+// EB: bytes per input element (2: fp16/bf16; 1: E4M3).  A swizzle chunk is
+// 128 bytes of a row: 64 16-bit or 128 8-bit columns.
+template <int D, int QT, int NS, int EB = 2>
 struct FwdLayout {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int kTileBytes = kBM * D * 2;
+  static_assert(EB == 2 || (EB == 1 && D == 128), "8-bit inputs: head dim 128");
+  static constexpr int kTileBytes = kBM * D * EB;
+  static constexpr int kChunkCols = 128 / EB;
+  static constexpr int kChunks = D / kChunkCols;
+  static constexpr int kK = 32 / EB;  // K elements per MMA (32 bytes of a row)
   static constexpr int kQ = 0;
   static constexpr int kKV = kQ + QT * kTileBytes;
   static constexpr int kBars = kKV + NS * kTileBytes;
@@ -235,14 +242,43 @@ __device__ __forceinline__ float2 unpack2(uint32_t v) {
   }
 }
 
-template <int D, int QT, int NS, bool CAUSAL, bool BF16>
+// Four fp32 values to E4M3 (nearest-even, saturating at 448), packed so that
+// byte j holds value j (the order a kind::f8f6f4 MMA reads K from TMEM).
+__device__ __forceinline__ uint32_t pack4_e4m3(float p0, float p1, float p2, float p3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(p1), "f"(p0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(p3), "f"(p2));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+// The four E4M3 values of a packed word (as pack4_e4m3 makes it), summed
+// into two fp32 accumulators: two f16 pairs, one packed add, two
+// mixed-precision FMAs.
+__device__ __forceinline__ void add4_e4m3(uint32_t w, float& acc0, float& acc1) {
+  uint32_t h01, h23, h;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"((uint16_t)(w & 0xFFFFu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"((uint16_t)(w >> 16)));
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(h01), "r"(h23));
+  asm("{\n\t.reg .b16 lo, hi, one;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "mov.b16 one, 0x3C00;\n\t"
+      "fma.rn.f32.f16 %0, lo, one, %0;\n\t"
+      "fma.rn.f32.f16 %1, hi, one, %1;\n\t}"
+      : "+f"(acc0), "+f"(acc1) : "r"(h));
+}
+
+// BF16: the output type (and, for 16-bit inputs, the input type).  FP8:
+// E4M3 inputs with per-tensor scales (folded into scale_log2 and o_scale),
+// scores and P V on kind::f8f6f4 MMAs, P rounded to E4M3.
+template <int D, int QT, int NS, bool CAUSAL, bool BF16, bool FP8 = false>
 __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
     fattn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const FwdParams p) {
-  using L = FwdLayout<D, QT, NS>;
+  using L = FwdLayout<D, QT, NS, FP8 ? 1 : 2>;
   using W = FwdWarps<QT>;
+  static_assert(!FP8 || !L::kSepP, "8-bit inputs use the layout where P overwrites S");
   extern __shared__ uint8_t smem_raw[];
 
   const uint32_t base = ptx::smem_u32(smem_raw);
@@ -331,9 +367,9 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           const uint32_t qb = bar(L::bQFull + i);
           ptx::mbar_arrive_expect_tx(qb, L::kTileBytes);
 #pragma unroll
-          for (int c = 0; c < D / kSwizzleChunkCols; ++c)
+          for (int c = 0; c < L::kChunks; ++c)
             ptx::tma_load_3d(sQ + i * L::kTileBytes + c * kChunkBytes, &tm_q, qb,
-                             c * kSwizzleChunkCols, w.q_row0 + kBM * i, w.bh);
+                             c * L::kChunkCols, w.q_row0 + kBM * i, w.bh);
           ++q_uses[i];
         }
         for (int j = 0; ok && j < w.n_max; ++j) {
@@ -348,9 +384,9 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
             const uint32_t fb = bar(L::bKVFull + kv_idx);
             ptx::mbar_arrive_expect_tx(fb, L::kTileBytes);
 #pragma unroll
-            for (int c = 0; c < D / kSwizzleChunkCols; ++c)
+            for (int c = 0; c < L::kChunks; ++c)
               ptx::tma_load_3d(sKV + kv_idx * L::kTileBytes + c * kChunkBytes,
-                               kv == 0 ? &tm_k : &tm_v, fb, c * kSwizzleChunkCols,
+                               kv == 0 ? &tm_k : &tm_v, fb, c * L::kChunkCols,
                                j * kBN, w.bh);
             FATTN_TRACE_EV(k, j, 5 + kv);
             kv_filled |= 1u << kv_idx;
@@ -378,8 +414,10 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
     // an MMA, so everything it does between two MMA groups is tensor idle
     // time: that path is kept short.
     {
-      constexpr uint32_t kIdS = ptx::idesc_f16(BF16 ? 1 : 0, kBM, kBN, 0, 0);
-      constexpr uint32_t kIdPV = ptx::idesc_f16(BF16 ? 1 : 0, kBM, D, 0, 1);
+      constexpr uint32_t kIdS = FP8 ? ptx::idesc_e4m3(kBM, kBN, 0, 0)
+                                    : ptx::idesc_f16(BF16 ? 1 : 0, kBM, kBN, 0, 0);
+      constexpr uint32_t kIdPV = FP8 ? ptx::idesc_e4m3(kBM, D, 0, 1)
+                                     : ptx::idesc_f16(BF16 ? 1 : 0, kBM, D, 0, 1);
       uint32_t kv_idx = 0, kv_ph = 0;
       uint32_t kv_item = 0;  // separate-P layout: ring index of the next unit's K_0
       int q_uses[QT], p_cnt[QT], oe_cnt[QT], used[QT], s_issued[QT];
@@ -412,36 +450,38 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       const uint32_t q_lo = ptx::desc_sw128_lo(sQ, 16);
       const uint32_t k_lo = ptx::desc_sw128_lo(sKV, 16);
       const uint32_t v_lo = ptx::desc_sw128_lo(sKV, kChunkBytes);  // LBO: next 64 columns
-      // S_i = Q_i K^T: M = 128, N = 128, K = D in steps of 16 (32 bytes of a
-      // 128-byte swizzled row; the next 64 columns are one chunk further).
+      // S_i = Q_i K^T: M = 128, N = 128, K = D in steps of kK (32 bytes of a
+      // 128-byte swizzled row; the next 128 bytes of the row are one chunk
+      // further).
       auto issue_s = [&](int i, uint32_t k_slot) {
         const uint32_t d = tmem + L::colS(i);
         const uint32_t qa = q_lo + i * kTileLo;
         const uint32_t kb = k_lo + k_slot * kTileLo;
         if (!ptx::elect_one()) return;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D / L::kK; ++kk) {
           const uint32_t off = ((kk / 4) * kChunkBytes + (kk % 4) * 32) >> 4;
           if (kk == 0)
-            ptx::mma_ss_lohi<0>(d, qa + off, kb + off, kHi, kIdS, 0u);
+            ptx::mma_ss_lohi<0, FP8>(d, qa + off, kb + off, kHi, kIdS, 0u);
           else
-            ptx::mma_ss_lohi<1>(d, qa + off, kb + off, kHi, kIdS, 1u);
+            ptx::mma_ss_lohi<1, FP8>(d, qa + off, kb + off, kHi, kIdS, 1u);
         }
       };
-      // O_i += P_i V: M = 128, N = D, K = 128 keys in steps of 16.  P_i is
-      // read from TMEM (two 16-bit values per column); V is MN-major, each
-      // step 16 key rows (2048 bytes) further.
+      // O_i += P_i V: M = 128, N = D, K = 128 keys in steps of kK.  P_i is
+      // read from TMEM (two 16-bit or four 8-bit values per column: 8
+      // columns per step); V is MN-major, each step kK key rows further.
       auto issue_pv = [&](int i, uint32_t v_slot, bool acc) {
         const uint32_t d = tmem + L::colO(i);
         const uint32_t a = tmem + L::colP(i);
         const uint32_t vb = v_lo + v_slot * kTileLo;
         if (!ptx::elect_one()) return;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
+        for (int kk = 0; kk < kBN / L::kK; ++kk) {
           if (kk == 0)
-            ptx::mma_ts_lohi<0>(d, a, vb, kHi, kIdPV, acc ? 1u : 0u);
+            ptx::mma_ts_lohi<0, FP8>(d, a, vb, kHi, kIdPV, acc ? 1u : 0u);
           else
-            ptx::mma_ts_lohi<1>(d, a + kk * 8, vb + kk * (2048 >> 4), kHi, kIdPV, 1u);
+            ptx::mma_ts_lohi<1, FP8>(d, a + kk * 8, vb + kk * ((L::kK * 128) >> 4), kHi,
+                                     kIdPV, 1u);
         }
       };
 
@@ -618,8 +658,10 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
     // FFMA per pair; 16-bit P goes to TMEM over the S columns (the whole row
     // is in registers), the row sum runs in four packed partial sums, and
     // with TRACK the row maximum of s is taken on the side.
+    // With FP8 also the sum of the weights as rounded to E4M3 (rsum): the
+    // normaliser of O, so that O is exactly a convex combination of V rows.
     auto exp_pass = [&](const float (&s)[kBN], float mref, uint32_t addr, auto track_c,
-                        float& tmax) -> float {
+                        float& tmax, float& rsum) -> float {
       constexpr bool kTrack = decltype(track_c)::value;
       const float2 c2 = make_float2(c, c);
       const float2 neg2 = make_float2(-mref, -mref);
@@ -629,9 +671,11 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       for (int a = 0; a < 4; ++a) sum2[a] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int a = 0; a < 8; ++a) acc[a] = -INFINITY;
+      float r0 = 0.f, r1 = 0.f;
 #pragma unroll
       for (int ch = 0; ch < kBN / 32; ++ch) {
         uint32_t pk[16];
+        float2 prev = make_float2(0.f, 0.f);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float s0 = s[ch * 32 + 2 * e], s1 = s[ch * 32 + 2 * e + 1];
@@ -639,13 +683,29 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           const float2 x = __ffma2_rn(make_float2(s0, s1), c2, neg2);
           const float2 pp = make_float2(ex2(x.x), ex2(x.y));
           sum2[e & 3] = __fadd2_rn(sum2[e & 3], pp);
-          pk[e] = pack2<BF16>(pp.x, pp.y);
+          if constexpr (FP8) {
+            if (e & 1) {
+              pk[e / 2] = pack4_e4m3(prev.x, prev.y, pp.x, pp.y);
+              add4_e4m3(pk[e / 2], r0, r1);
+            }
+            prev = pp;
+          } else {
+            pk[e] = pack2<BF16>(pp.x, pp.y);
+          }
         }
-        ptx::tmem_st16(addr + ch * 16, pk);
+        if constexpr (FP8) {
+          uint32_t p8[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) p8[e] = pk[e];
+          ptx::tmem_st8(addr + ch * 8, p8);
+        } else {
+          ptx::tmem_st16(addr + ch * 16, pk);
+        }
       }
       if (kTrack)
         tmax = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
                      fmaxf(acc[6], acc[7]));
+      if constexpr (FP8) rsum = r0 + r1;
       const float2 s4 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
       return s4.x + s4.y;
     };
@@ -719,7 +779,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
 #pragma unroll
           for (int e = 0; e < kBN; ++e) s[e] = e < limit ? s[e] : -INFINITY;
         }
-        float m_use = m, alpha = 1.0f, sum, tmax;
+        float m_use = m, alpha = 1.0f, sum, tmax, rsum = 0.f;
         if constexpr (L::kSepP) {
           // Separate P: the maximum first (no redo is possible once packed P
           // waits in registers for its buffer), then the exponents.
@@ -783,7 +843,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           }
           FATTN_TRACE_EV(k, j, 8 * i + 3);
           tmax = -INFINITY;
-          sum = exp_pass(s, m_use, s_addr, std::true_type{}, tmax);
+          sum = exp_pass(s, m_use, s_addr, std::true_type{}, tmax, rsum);
           if (j > 0) {
             const float mxc = tmax * c;
             const bool move = mxc > m + kRescaleLog2;
@@ -792,7 +852,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                 m_use = mxc;
                 alpha = ex2(m - m_use);
               }
-              sum = exp_pass(s, m_use, s_addr, std::false_type{}, tmax);
+              sum = exp_pass(s, m_use, s_addr, std::false_type{}, tmax, rsum);
             }
           }
         }
@@ -822,10 +882,14 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         // peaked row's dominant weight exact, as p = 1 would be under an
         // exact running maximum.  (fmaf gives the same value as a lane of
         // the packed FFMA above.)
-        const float pt = ex2(fmaf(tmax, c, -m_use));
-        const float pt16 = unpack2<BF16>(pack2<BF16>(pt, 0.f)).x;
         l = alpha * l + sum;
-        lr = alpha * lr + (sum + (pt16 - pt));
+        if constexpr (FP8) {
+          lr = alpha * lr + rsum;
+        } else {
+          const float pt = ex2(fmaf(tmax, c, -m_use));
+          const float pt16 = unpack2<BF16>(pack2<BF16>(pt, 0.f)).x;
+          lr = alpha * lr + (sum + (pt16 - pt));
+        }
         m = m_use;
       }
       if (!ok) break;
@@ -878,7 +942,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         if (!wait_all(L::bPVDone + i, (uint32_t)(pv_base[i] + n[i] - 1) & 1u)) { ok = false; break; }
         pv_base[i] += n[i];
         ptx::tc_fence_after();
-        const float inv_l = 1.0f / l;
+        const float inv_l = p.o_scale / l;
         const int row = w.q_row0 + kBM * i + r;
         const bool valid = row < p.S;
         const size_t grow = (size_t)w.bh * (size_t)p.S + (size_t)row;

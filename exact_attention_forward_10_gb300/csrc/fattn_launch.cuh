@@ -66,6 +66,33 @@ cudaError_t launch_fwd(const LaunchArgs& a) {
   return cudaGetLastError();
 }
 
+// E4M3 inputs, head dim 128: 16 KB tiles leave room for a 12-stage ring.
+constexpr int kFp8Stages = 12;
+struct Fp8Shape {
+  using L = FwdLayout<128, 2, kFp8Stages, 1>;
+  static constexpr int kSmem = L::kSmemBytes;
+  static constexpr int kThreads = FwdWarps<2>::kThreads;
+  static_assert(kSmem <= 232448, "shared memory per CTA");
+};
+
+template <bool CAUSAL, bool BF16>
+cudaError_t launch_fwd_fp8(const LaunchArgs& a) {
+  auto kern = &fattn_fwd_kernel<128, 2, kFp8Stages, CAUSAL, BF16, true>;
+  static volatile bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Fp8Shape::kSmem);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) attr_set[dev] = true;
+  }
+  kern<<<a.grid, Fp8Shape::kThreads, Fp8Shape::kSmem, a.stream>>>(*a.tm_q, *a.tm_k,
+                                                                  *a.tm_v, a.params);
+  return cudaGetLastError();
+}
+
 // Head dim 256: the CTA-pair kernel (clusters of two CTAs, one per SM).
 constexpr int kPairStages = 5;
 struct PairShape {
@@ -130,6 +157,7 @@ int pair_clusters_fit() {
 cudaError_t launch_fwd_d64(bool causal, bool bf16, const LaunchArgs& a);
 cudaError_t launch_fwd_d128(bool causal, bool bf16, const LaunchArgs& a);
 cudaError_t launch_fwd_d256(bool causal, bool bf16, const LaunchArgs& a);
+cudaError_t launch_fwd_fp8_d128(bool causal, bool bf16_out, const LaunchArgs& a);
 int pair_clusters_d256(bool causal, bool bf16);
 
 }  // namespace fattn

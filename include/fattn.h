@@ -86,6 +86,34 @@ FATTN_API int fattn_fwd(const void *q, const void *k, const void *v, void *o,
                         float scale, int dtype, fattn_stream_t stream);
 
 /*
+ * Attention forward with 8-bit inputs ("FlashAttention V2", section 7: FP8
+ * attention on the FP8 tensor cores).  The same operation as fattn_fwd on the
+ * real values Q = q_scale * Q8, K = k_scale * K8, V = v_scale * V8:
+ *   O = softmax(scale * Q K^T [+ causal]) V,  LSE = natural-log LSE of the
+ *   scaled scores.
+ * Scores and P V run on kind::f8f6f4 tensor-core MMAs; P is rounded to E4M3
+ * before the P V product and O is normalised by the sum of those rounded
+ * weights (a convex combination of V rows), so O carries the E4M3 rounding
+ * of the attention weights (relative 2^-4, absolute 2^-10 below the E4M3
+ * normal range, weights taken relative to the row maximum); the LSE uses the
+ * fp32 sum of the unrounded weights and does not.
+ *
+ *   q, k, v    device [B, H, S, D] E4M3 codes (OCP "fn" format: bias 7, three
+ *              mantissa bits, largest 448), one byte each, 16-byte aligned
+ *   o          device [B, H, S, D] output of out_dtype, 16-byte aligned
+ *   lse        device [B, H, S] fp32, 4-byte aligned
+ *   D          128
+ *   scale      score multiplier on the real values, finite and > 0
+ *   q_scale, k_scale, v_scale   per-tensor dequantisation scales, finite > 0
+ *   out_dtype  FATTN_FP16 or FATTN_BF16
+ * Other arguments, layout, ownership and errors as fattn_fwd.
+ */
+FATTN_API int fattn_fwd_fp8(const void *q, const void *k, const void *v, void *o,
+                            float *lse, int B, int H, int S, int D, int causal,
+                            float scale, float q_scale, float k_scale,
+                            float v_scale, int out_dtype, fattn_stream_t stream);
+
+/*
  * Synchronises ``stream``, then reads and clears the current device's status
  * block.  Returns FATTN_OK, FATTN_ERR_PIPELINE_TIMEOUT (a kernel gave up on a
  * wait and unwound; its outputs are incomplete), FATTN_ERR_LAUNCH (a kernel

@@ -172,3 +172,73 @@ def check_kvcache(x: attn_inputs.KVCache, causal: bool, label: str = "",
     o, lse = run_cuda_kvcache(x, causal, scale, stale_nan=stale_nan)
     ro, rl = oracle.attn_kvcache(x.q, x.k, x.v, causal, scale, x.lens)
     return compare_kvcache(o, lse, ro, rl, x.dtype, label)
+
+
+# ------------------------------------------------------ E4M3 (FP8) inputs
+
+def fp8_bound(x: attn_inputs.QKV8, causal: bool, scale: float):
+    """fp64 oracle result and a per-element error bound for the FP8 path.
+
+    The kernel rounds every attention weight to E4M3 before P V: for weights
+    normalised to the row maximum, |p~ - p| <= max(2^-4 p, 2^-10) (relative
+    half-ulp in the normal range, half the subnormal quantum below it; the
+    lazy reference maximum only rescales p by 2^0..2^8, which keeps both
+    limits).  The kernel normalises by the sum of the rounded weights, so O =
+    sum w~_j v_j with w~ = p~ / sum p~, and with e_j = max(2^-4 p_j, 2^-10),
+    L = sum p_j >= 1 (the maximum contributes 1) and sum p~ >= L (1 - 2^-4):
+      |O - O_ref| = |sum (w~_j - w_j)(v_j - O_ref)|
+                  <= (16/15) [sum e_j |v_j - O_ref| + (sum e_j) M] / L,
+    M = sum_j w_j |v_j - O_ref|; plus the 16-bit output rounding (2^-8 |O|)
+    and 1e-5 for fp32 accumulation and ex2.  Returns (O_ref, LSE_ref, tol),
+    numpy fp64, for inputs small enough for the whole P."""
+    ro, rl, P = oracle.attn_fwd_numpy(x.q, x.k, x.v, causal, scale, want_p=True)
+    return ro, rl, _fp8_tol(P, x.v, ro)
+
+
+def _fp8_tol(P, v, ro):
+    """The bound of fp8_bound from probabilities P [..., i, j], values v
+    [..., j, d] and the reference output ro [..., i, d]."""
+    pn = P / P.max(axis=-1, keepdims=True)      # weights relative to the row max
+    err_w = np.maximum(2.0 ** -4 * pn, np.where(pn > 0, 2.0 ** -10, 0.0))
+    L = pn.sum(axis=-1)
+    dev = np.abs(v[..., None, :, :] - ro[..., :, None, :])  # [..., i, j, d]
+    M = np.einsum("...ij,...ijd->...id", pn / L[..., None], dev)
+    tol = (16.0 / 15.0) * (np.einsum("...ij,...ijd->...id", err_w, dev) +
+                           err_w.sum(axis=-1)[..., None] * M) / L[..., None]
+    return tol + 2.0 ** -8 * np.abs(ro) + 1e-5
+
+
+def fp8_bound_rows(x: attn_inputs.QKV8, causal: bool, scale: float, bh: int, rows):
+    """fp8_bound for some query rows of head ``bh`` (long sequences): the
+    definition in fp64 numpy on those rows only."""
+    B, H, S, D = x.q.shape
+    b, h = divmod(bh, H)
+    rows = np.asarray(rows)
+    s = scale * (x.q[b, h, rows] @ x.k[b, h].T)          # [n, S]
+    if causal:
+        s = np.where(np.arange(S)[None, :] <= rows[:, None], s, -np.inf)
+    m = s.max(axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    l = e.sum(axis=-1, keepdims=True)
+    P = e / l
+    ro = P @ x.v[b, h]
+    rl = (m + np.log(l))[:, 0]
+    return ro, rl, _fp8_tol(P, x.v[b, h], ro)
+
+
+def run_cuda_fp8(x: attn_inputs.QKV8, causal: bool, scale: float, out_dtype: str = "bf16"):
+    import torch
+
+    import exact_attention_forward_10_gb300 as fattn
+
+    dev = torch.device("cuda:0")
+    q8, k8, v8 = (torch.from_numpy(a).to(dev) for a in (x.q8, x.k8, x.v8))
+    B, H, S, D = q8.shape
+    o = torch.full((B, H, S, D), float("nan"), dtype=torch_dtype(out_dtype), device=dev)
+    lse = torch.full((B, H, S), float("nan"), dtype=torch.float32, device=dev)
+    fattn.forward_fp8(q8, k8, v8, *x.descale, causal=causal, scale=scale,
+                      out_dtype=torch_dtype(out_dtype), out=o, lse=lse)
+    torch.cuda.synchronize()
+    rc, where = fattn.fattn_last_error(0)
+    assert rc == 0, f"kernel status {rc} ({fattn.fattn_error_string(rc)}) at {where}"
+    return o.double().cpu().numpy(), lse.double().cpu().numpy()

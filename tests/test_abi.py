@@ -130,3 +130,26 @@ def test_kvcache_host_side_rejections(lib, args, want):
                                  a["D"], a["causal"], a["scale"], a["dtype"],
                                  a["ws"], a["ws_bytes"], a["stream"])
     assert rc == want
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(q=0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(qs=-1.0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(vs=float("inf")), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(S=0), fattn.FATTN_ERR_INVALID_ARG),
+    (dict(D=64), fattn.FATTN_ERR_UNSUPPORTED),
+    (dict(D=256), fattn.FATTN_ERR_UNSUPPORTED),
+    (dict(out=3), fattn.FATTN_ERR_UNSUPPORTED),
+    (dict(k=P * 3 + 4), fattn.FATTN_ERR_MISALIGNED),
+    (dict(lse=P * 11 + 2), fattn.FATTN_ERR_MISALIGNED),
+    (dict(o=P), fattn.FATTN_ERR_INVALID_ARG),      # o overlaps q
+])
+def test_fp8_host_side_rejections(lib, args, want):
+    a = dict(q=P, k=P * 3, v=P * 7, o=P * 9, lse=P * 11, B=1, H=2, S=256, D=128,
+             causal=0, scale=0.088, qs=0.5, ks=0.5, vs=0.5, out=1, stream=0)
+    a.update(args)
+    rc = fattn.fattn_fwd_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"],
+                             a["S"], a["D"], a["causal"], a["scale"], a["qs"], a["ks"],
+                             a["vs"], a["out"], a["stream"])
+    assert rc == want

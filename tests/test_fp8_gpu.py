@@ -1,0 +1,113 @@
+"""E4M3 inputs (the FP8 forward) vs the fp64 oracle on the real values, through
+the C ABI.  Every element must lie within the bound derived in
+``parity.fp8_bound`` (the E4M3 rounding of the attention weights); the LSE
+within 1e-3.  Special inputs where that rounding is exact (zero queries:
+every weight 1; constant V rows) must match to the output rounding."""
+import math
+
+import numpy as np
+import pytest
+
+import attn_inputs
+from parity import fp8_bound, fp8_bound_rows, run_cuda_fp8, sample_rows
+
+pytestmark = pytest.mark.gpu
+SCALE = 1.0 / math.sqrt(128)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _check(o, lse, ro, rl, tol, label):
+    assert np.isfinite(o).all() and np.isfinite(lse).all(), f"{label}: unwritten output"
+    err = np.abs(o - ro)
+    bad = err > tol
+    if bad.any():
+        idx = np.unravel_index(np.argmax(np.where(bad, err - tol, -np.inf)), err.shape)
+        raise AssertionError(f"{label}: {int(bad.sum())} elements outside the bound; "
+                             f"at {idx} got {o[idx]}, want {ro[idx]}, bound {tol[idx]:.3e}")
+    e_l = float(np.abs(lse - rl).max())
+    assert e_l <= 1e-3, f"{label}: max|dLSE| = {e_l:.3e}"
+    return float(err.max()), float((err / tol).max())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("out", ["bf16", "fp16"])
+@pytest.mark.parametrize("S", [1, 2, 127, 128, 129, 300, 513])
+def test_small_and_ragged(S, out, causal):
+    x = attn_inputs.make_qkv_fp8(1, 2, S, 128, seed=6000 + S)
+    o, lse = run_cuda_fp8(x, causal, SCALE, out)
+    ro, rl, tol = fp8_bound(x, causal, SCALE)
+    _check(o, lse, ro, rl, tol, f"fp8 S{S} {out} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_head_multi_tile(causal):
+    x = attn_inputs.make_qkv_fp8(2, 3, 1000, 128, seed=6100)
+    o, lse = run_cuda_fp8(x, causal, SCALE)
+    ro, rl, tol = fp8_bound(x, causal, SCALE)
+    _check(o, lse, ro, rl, tol, f"fp8 B2 H3 S1000 causal={causal}")
+
+
+def test_large_scores():
+    """Q, K x 4 before quantisation: the running maximum moves a lot."""
+    x = attn_inputs.make_qkv_fp8(1, 4, 777, 128, seed=6200, qk_mult=4.0)
+    for causal in (False, True):
+        o, lse = run_cuda_fp8(x, causal, SCALE)
+        ro, rl, tol = fp8_bound(x, causal, SCALE)
+        _check(o, lse, ro, rl, tol, f"fp8 x4 causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_queries_give_exact_means(causal):
+    """Q = 0: every weight is exactly 1 (exact in E4M3), so O is the mean of
+    the allowed V rows up to fp32 summation and the output rounding."""
+    x = attn_inputs.make_qkv_fp8(1, 3, 700, 128, seed=6300)
+    x.q8[:] = 0
+    x.q[:] = 0
+    o, lse = run_cuda_fp8(x, causal, SCALE)
+    S = 700
+    cnt = np.arange(1, S + 1) if causal else np.full(S, S)
+    want = (np.cumsum(x.v, axis=2) / cnt[None, None, :, None] if causal
+            else np.broadcast_to(x.v.mean(axis=2, keepdims=True), x.v.shape))
+    np.testing.assert_allclose(o, want, rtol=2.0 ** -8, atol=1e-5)
+    np.testing.assert_allclose(lse, np.broadcast_to(np.log(cnt), lse.shape), atol=1e-5)
+
+
+def test_constant_value_rows():
+    """Every V row equal: O is that row whatever the weights."""
+    x = attn_inputs.make_qkv_fp8(2, 2, 400, 128, seed=6400)
+    x.v8[:] = x.v8[0, 0, :1]
+    x.v[:] = x.v[0, 0, :1]
+    for causal in (False, True):
+        o, _ = run_cuda_fp8(x, causal, SCALE)
+        np.testing.assert_allclose(o, np.broadcast_to(x.v[0, 0, 0], o.shape),
+                                   rtol=2.0 ** -8, atol=1e-5)
+
+
+@pytest.mark.parametrize("S", [4097, 8192])
+def test_long_sequences_sampled(S):
+    x = attn_inputs.make_qkv_fp8(2, 16, S, 128, seed=6500 + S)
+    for causal in (False, True):
+        o, lse = run_cuda_fp8(x, causal, SCALE)
+        rows = sample_rows(2, 16, S, seed=S, n_heads=3, stride=256)
+        for bh in sorted(set((rows // S).tolist())):
+            r = rows[rows // S == bh] % S
+            ro, rl, tol = fp8_bound_rows(x, causal, SCALE, bh, r)
+            b, h = divmod(bh, 16)
+            _check(o[b, h, r], lse[b, h, r], ro, rl, tol,
+                   f"fp8 B2 H16 S{S} head {bh} causal={causal}")
+
+
+def test_deterministic():
+    x = attn_inputs.make_qkv_fp8(2, 4, 900, 128, seed=6600)
+    o1, l1 = run_cuda_fp8(x, True, SCALE)
+    o2, l2 = run_cuda_fp8(x, True, SCALE)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)

@@ -1,5 +1,7 @@
 """The seeded input generator: published SplitMix64 outputs, Box-Muller
 statistics, exact rounding to the 16-bit dtypes and the workload seeds."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -83,3 +85,48 @@ def test_cache_inputs_follow_the_stream():
     assert ai.make_kvcache(1, 1, 1, 4, 8, "bf16", 1).lens is None
     with pytest.raises(ValueError):
         ai.make_kvcache(1, 1, 1, 4, 8, "bf16", 1, (1, 5))
+
+
+def test_e4m3_codes_round_trip_and_ties():
+    """Every finite E4M3 code decodes and re-encodes to itself; midpoints
+    between neighbours round to the even mantissa; large values saturate."""
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    vals = ai.e4m3_decode(codes)
+    back = ai.e4m3_encode(vals)
+    # -0 and +0 both encode as +0
+    assert np.array_equal(back[vals != 0], codes[vals != 0])
+    assert ai.e4m3_decode(np.array([0x7E]))[0] == 448.0
+    assert ai.e4m3_decode(np.array([0x38]))[0] == 1.0
+    assert ai.e4m3_decode(np.array([0x01]))[0] == 2.0 ** -9
+    pos = np.sort(ai.e4m3_decode(np.arange(0, 0x7F)))
+    mid = (pos[1:] + pos[:-1]) / 2
+    lo = ai.e4m3_encode(mid)
+    even = np.where((ai.e4m3_encode(pos[:-1]) & 1) == 0, ai.e4m3_encode(pos[:-1]),
+                    ai.e4m3_encode(pos[1:]))
+    assert np.array_equal(lo, even)
+    assert ai.e4m3_decode(ai.e4m3_encode(np.array([1e6, -500.0, 464.0])))[0] == 448.0
+    assert ai.e4m3_decode(ai.e4m3_encode(np.array([-500.0])))[0] == -448.0
+
+
+def test_e4m3_matches_torch_cast_inside_range():
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    if f8 is None:
+        pytest.skip("torch has no float8_e4m3fn")
+    x = ai.normals(11, 0, 50000) * 40.0
+    x = x[np.abs(x) < 440]
+    got = ai.e4m3_decode(ai.e4m3_encode(x))
+    want = torch.from_numpy(x).to(f8).to(torch.float64).numpy()
+    np.testing.assert_array_equal(got, want)
+
+
+def test_fp8_inputs_dequantise_exactly():
+    x = ai.make_qkv_fp8(1, 2, 64, 128, seed=5)
+    for codes, scale, real in ((x.q8, x.descale[0], x.q), (x.v8, x.descale[2], x.v)):
+        assert codes.dtype == np.uint8 and codes.shape == (1, 2, 64, 128)
+        np.testing.assert_array_equal(ai.e4m3_decode(codes) * scale, real)
+        assert np.abs(ai.e4m3_decode(codes)).max() <= 448
+        assert math.log2(scale) == int(math.log2(scale))
+    # the same normals as the 16-bit generator, before rounding
+    z = ai.normals(5, 0, 64 * 128 * 2)
+    rel = np.abs(x.q.reshape(-1) - z) / np.maximum(np.abs(z), 2 ** -6 * x.descale[0])
+    assert rel.max() <= 2 ** -4 + 1e-12
