@@ -487,6 +487,158 @@ def run_sweep(args):
     return 0
 
 
+# ------------------------------------------------------ E4M3 (FP8) inputs
+
+def run_fp8(args):
+    """One step = the non-causal and the causal FP8 forward of the benchmark
+    shape (B2 H16 S8192 D128; Q, K, V the seed-3 normals quantised to E4M3
+    per tensor), bf16 output, inputs resident in HBM."""
+    import torch
+
+    import exact_attention_forward_10_gb300 as fattn
+
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    w = WORKLOAD
+    x = attn_inputs.make_qkv_fp8(w.B, w.H, w.S, w.D, w.seed)
+    host = [torch.from_numpy(a).pin_memory() for a in (x.q8, x.k8, x.v8)]
+    q, k, v = (h.to(dev) for h in host)
+    B, H, S, D = w.B, w.H, w.S, w.D
+    outs = {c: (torch.empty((B, H, S, D), dtype=torch.bfloat16, device=dev),
+                torch.empty((B, H, S), dtype=torch.float32, device=dev)) for c in MASKS}
+    stream = torch.cuda.Stream(dev)
+    sptr = stream.cuda_stream
+    qs, ks, vs = x.descale
+
+    def launch(causal, qq, kk, vv):
+        o, l = outs[causal]
+        rc = fattn.fattn_fwd_fp8(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
+                                 l.data_ptr(), B, H, S, D, causal, w.scale, qs, ks, vs,
+                                 fattn.FATTN_BF16, sptr)
+        if rc != 0:
+            raise fattn.FattnError(rc, "fattn_fwd_fp8")
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    with torch.cuda.stream(stream):
+        for c in MASKS:
+            launch(c, q, k, v)
+        for _ in range(args.warmup):
+            for c in MASKS:
+                launch(c, q, k, v)
+    rc, where = fattn.fattn_last_error(sptr)
+    if rc != 0:
+        raise RuntimeError(f"kernel status {rc} at {where}")
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps * len(MASKS))]
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.25)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        e = 0
+        for _ in range(args.steps):
+            for c in MASKS:
+                ev[e][0].record(stream)
+                launch(c, q, k, v)
+                ev[e][1].record(stream)
+                e += 1
+        t1.record(stream)
+    barrier()
+    clocks = sampler.stop()
+    rc, where = fattn.fattn_last_error(sptr)
+    if rc != 0:
+        raise RuntimeError(f"kernel status {rc} at {where}")
+    per_launch = {c: [] for c in MASKS}
+    for i, (a, b) in enumerate(ev):
+        per_launch[MASKS[i % len(MASKS)]].append(a.elapsed_time(b))
+    step_ms = t0.elapsed_time(t1) / args.steps
+
+    h_outs = {c: (torch.empty((B, H, S, D), dtype=torch.bfloat16).pin_memory(),
+                  torch.empty((B, H, S), dtype=torch.float32).pin_memory()) for c in MASKS}
+
+    def e2e_step():
+        qq, kk, vv = (h.to(dev, non_blocking=True) for h in host)
+        for c in MASKS:
+            launch(c, qq, kk, vv)
+        for c in MASKS:
+            h_outs[c][0].copy_(outs[c][0], non_blocking=True)
+            h_outs[c][1].copy_(outs[c][1], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+    barrier()
+    n_e2e = max(3, min(args.steps, 20))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([step_ms, e2e_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, e2e_ms = float(t[0]), float(t[1])
+    flops_step = sum(metric_flops(B, H, S, D, c) for c in MASKS)
+    peaks = load_peaks()
+    peak8 = 2.0 * peaks["burst"]
+    per_mask = {}
+    for c in MASKS:
+        ms = statistics.median(per_launch[c])
+        tf = metric_flops(B, H, S, D, c) / (ms * 1e-3) / 1e12
+        per_mask["causal" if c else "noncausal"] = {"ms_median": ms, "tflops": tf,
+                                                     "frac_of_fp8_peak": tf / peak8}
+    achieved = metric_flops(B, H, S, D, False) / (statistics.mean(per_launch[False]) * 1e-3) / 1e12
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(x, w)
+        print(json.dumps({
+            "metric": METRIC + " (E4M3 inputs, against the FP8 peak)",
+            "value": world * flops_step / (step_ms * 1e-3) / 1e12, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
+            "config": workload_config(w, {"inputs": "E4M3 codes, per-tensor power-of-two "
+                                                    "scales", "output": "bf16",
+                                          "parallelism": f"replicas x{world}"}),
+            "per_mask": per_mask,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak8,
+                         "unit": "TFLOP/s", "frac": achieved / peak8,
+                         "peak_kind": (f"fp8 dense = 2 x the {peaks['source']} bf16 burst "
+                                       "(nominal fp8/bf16 ratio 4.5/2.25)"),
+                         "kernel": "fattn_fwd_kernel<D=128, non-causal, E4M3 in, bf16 out>",
+                         "traffic": None},
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": sum(h.numel() for h in host),
+                    "d2h_bytes_per_step": sum(o.numel() * 2 + l.numel() * 4
+                                              for o, l in h_outs.values()),
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * len(MASKS),
+            "clocks": clocks}), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
 # ------------------------------------------- attention against a KV cache
 
 KV_METRIC = ("decode attention against a KV cache: effective HBM GB/s "
@@ -749,6 +901,8 @@ def main():
     ap.add_argument("--dims", default="64,128",
                     help="head dims of --sweep (64,128 are the sweep's; 256 adds the "
                          "CTA-pair kernel)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the E4M3-input forward on the step workload (D=128)")
     ap.add_argument("--kvcache", nargs="?", const="decode_b16_h16_d128_ragged",
                     default=None, choices=sorted(attn_inputs.CACHE_WORKLOADS),
                     help="time attention of new queries against a KV cache "
@@ -777,6 +931,10 @@ def main():
         args.warmup = 3
     if args.sweep:
         return run_sweep(args)
+    if args.fp8:
+        if WORKLOAD.D != 128:
+            ap.error("--fp8 needs head dim 128")
+        return run_fp8(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_fattn(args)
