@@ -6,13 +6,13 @@ namespace fattn {
 
 cudaError_t launch_fwd_d256(bool causal, bool bf16, const LaunchArgs& a) {
   if (causal)
-    return bf16 ? launch_fwd_pair<true, true>(a) : launch_fwd_pair<true, false>(a);
-  return bf16 ? launch_fwd_pair<false, true>(a) : launch_fwd_pair<false, false>(a);
+    return bf16 ? launch_fwd_pair<256, true, true>(a) : launch_fwd_pair<256, true, false>(a);
+  return bf16 ? launch_fwd_pair<256, false, true>(a) : launch_fwd_pair<256, false, false>(a);
 }
 
 int pair_clusters_d256(bool causal, bool bf16) {
-  if (causal) return bf16 ? pair_clusters_fit<true, true>() : pair_clusters_fit<true, false>();
-  return bf16 ? pair_clusters_fit<false, true>() : pair_clusters_fit<false, false>();
+  if (causal) return bf16 ? pair_clusters_fit<256, true, true>() : pair_clusters_fit<256, true, false>();
+  return bf16 ? pair_clusters_fit<256, false, true>() : pair_clusters_fit<256, false, false>();
 }
 
 }  // namespace fattn

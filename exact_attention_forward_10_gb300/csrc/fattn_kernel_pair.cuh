@@ -51,17 +51,20 @@
 namespace fattn {
 namespace pair {
 
-constexpr int kD = 256;
 constexpr int kRows = 2 * kBM;          // query rows per unit (the pair)
-constexpr int kItemBytes = 32768;       // one K half or one V half
-constexpr int kQBytes = kBM * kD * 2;   // this CTA's Q tile
 constexpr int kQChunk = kBM * 128;      // [128 rows, 64 cols]
 constexpr int kKChunk = 64 * 128;       // [64 keys, 64 cols]
 constexpr int kVChunk = kBN * 128;      // [128 keys, 64 cols]
 constexpr uint16_t kBoth = 3;           // multicast mask: both CTAs
 
-template <int NS>
+// D: head dim (128 or 256).  NSB: TMEM score buffers (P overwrites the
+// first 64 columns of one); O takes D columns after them.  NS: K/V ring items.
+template <int D, int NSB, int NS>
 struct PairLayout {
+  static_assert(D == 128 || D == 256, "head dim");
+  static_assert(128 * NSB + D <= (int)kTmemCols, "TMEM budget");
+  static constexpr int kQBytes = kBM * D * 2;      // this CTA's Q tile
+  static constexpr int kItemBytes = 128 * D;       // one K half or one V half
   static constexpr int kQ = 0;
   static constexpr int kKV = kQ + kQBytes;
   static constexpr int kBars = kKV + NS * kItemBytes;
@@ -69,10 +72,11 @@ struct PairLayout {
   static constexpr int bQEmpty = 1;         // each CTA: pair commit
   static constexpr int bKVFull = 2;         // rank 0: 1 arrival + both halves
   static constexpr int bKVEmpty = bKVFull + NS;   // each CTA: pair commit
-  static constexpr int bSFull = bKVEmpty + NS;    // [2] each CTA: pair commit
-  static constexpr int bPFull = bSFull + 2;       // [2] rank 0: 8 warp arrivals
-  static constexpr int bPVDone = bPFull + 2;      // each CTA: pair commit per PV
-  static constexpr int bODone = bPVDone + 1;      // each CTA: pair commit per unit
+  static constexpr int bSFull = bKVEmpty + NS;    // [NSB] each CTA: pair commit
+  static constexpr int bPFull = bSFull + NSB;     // [NSB] rank 0: 8 warp arrivals
+  static constexpr int bPVDone = bPFull + NSB;    // [NSB] each CTA: pair commit per PV
+                                                  // reading that buffer
+  static constexpr int bODone = bPVDone + NSB;    // each CTA: pair commit per unit
   static constexpr int bOEmpty = bODone + 1;      // rank 0: 8 warp arrivals
   static constexpr int bStats = bOEmpty + 1;      // each CTA: 128 arrivals
   static constexpr int bStatsFree = bStats + 1;   // each CTA: 4 warp arrivals
@@ -83,9 +87,8 @@ struct PairLayout {
   static constexpr int kRowM = kRowL + kBM * 4;
   static constexpr int kSmemBytes = kRowM + kBM * 4;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-  // TMEM: two score buffers (P overwrites the first 64 columns of one), O.
   __host__ __device__ static constexpr uint32_t colS(int b) { return 128u * b; }
-  static constexpr uint32_t kColO = 256;
+  static constexpr uint32_t kColO = 128u * NSB;
 };
 
 struct PairWarps {
@@ -142,13 +145,15 @@ __device__ __forceinline__ int pair_unit_of_round(int k) {
   return k * G + ((k & 1) ? (G - 1 - g) : g);
 }
 
-template <int NS, bool CAUSAL, bool BF16>
+template <int D, int NSB, int NS, bool CAUSAL, bool BF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads, 1)
     fattn_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v,
                           const FwdParams p) {
-  using L = PairLayout<NS>;
+  using L = PairLayout<D, NSB, NS>;
+  constexpr int kQBytes = L::kQBytes;
+  constexpr int kItemBytes = L::kItemBytes;
   using W = PairWarps;
   extern __shared__ uint8_t smem_raw[];
 
@@ -187,11 +192,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
       ptx::mbar_init(bar(L::bKVFull + s), 1);
       ptx::mbar_init(bar(L::bKVEmpty + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NSB; ++b) {
       ptx::mbar_init(bar(L::bSFull + b), 1);
       ptx::mbar_init(bar(L::bPFull + b), 8);
+      ptx::mbar_init(bar(L::bPVDone + b), 1);
     }
-    ptx::mbar_init(bar(L::bPVDone), 1);
     ptx::mbar_init(bar(L::bODone), 1);
     ptx::mbar_init(bar(L::bOEmpty), 8);
     ptx::mbar_init(bar(L::bStats), kBM);
@@ -244,7 +249,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
         }
         if (leader) ptx::mbar_arrive_expect_tx(bar(L::bQFull), 2 * kQBytes);
 #pragma unroll
-        for (int c = 0; c < kD / kSwizzleChunkCols; ++c)
+        for (int c = 0; c < D / kSwizzleChunkCols; ++c)
           ptx::tma_load_3d_pair(sQ + c * kQChunk, &tm_q, bar0(L::bQFull),
                                 c * kSwizzleChunkCols, w.row0 + kBM * (int)rank, w.bh);
         ++q_uses;
@@ -262,15 +267,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
             if (kv == 0) {
               // K half: keys [128 j + 64 rank, +64), all 256 columns
 #pragma unroll
-              for (int c = 0; c < kD / kSwizzleChunkCols; ++c)
+              for (int c = 0; c < D / kSwizzleChunkCols; ++c)
                 ptx::tma_load_3d_pair(dst + c * kKChunk, &tm_k, fb, c * kSwizzleChunkCols,
                                       j * kBN + 64 * (int)rank, w.bh);
             } else {
-              // V half: keys [128 j, +128), columns [128 rank, +128)
+              // V half: keys [128 j, +128), columns [D/2 rank, +D/2)
 #pragma unroll
-              for (int c = 0; c < 2; ++c)
+              for (int c = 0; c < D / 128; ++c)
                 ptx::tma_load_3d_pair(dst + c * kVChunk, &tm_v, fb,
-                                      128 * (int)rank + c * kSwizzleChunkCols, j * kBN, w.bh);
+                                      (D / 2) * (int)rank + c * kSwizzleChunkCols, j * kBN,
+                                      w.bh);
             }
             filled |= 1u << idx;
             fill_ph = (fill_ph & ~(1u << idx)) | (ph << idx);
@@ -296,14 +302,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
     // ------------------------------------------------------ MMA warp (rank 0)
     if (leader) {
       constexpr uint32_t kIdS = ptx::idesc_f16(BF16 ? 1 : 0, kRows, kBN, 0, 0);
-      constexpr uint32_t kIdPV = ptx::idesc_f16(BF16 ? 1 : 0, kRows, kD, 0, 1);
+      constexpr uint32_t kIdPV = ptx::idesc_f16(BF16 ? 1 : 0, kRows, D, 0, 1);
       constexpr uint32_t kHi = ptx::desc_sw128_hi(1024);
       constexpr uint32_t kItemLo = kItemBytes >> 4;
       const uint32_t q_lo = ptx::desc_sw128_lo(sQ, 16);
       const uint32_t k_lo = ptx::desc_sw128_lo(sKV, 16);
       const uint32_t v_lo = ptx::desc_sw128_lo(sKV, kVChunk);  // LBO: next 64 columns
       uint32_t item = 0;  // ring index of the next unit's K_0
-      int q_uses = 0, pf_cnt[2] = {0, 0}, oe_cnt = 0, used = 0;
+      int q_uses = 0, pf_cnt[NSB] = {}, oe_cnt = 0, used = 0;
       bool ok = true;
       auto wait_or_fail = [&](int slot, uint32_t parity) -> bool {
         bool w_ok = ptx::mbar_wait_cluster(bar(slot), parity, abort_flag, tmo);
@@ -322,7 +328,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
         const uint32_t kb = k_lo + slot * kItemLo;
         if (!ptx::elect_one()) return;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t qa = q_lo + (((kk / 4) * kQChunk + (kk % 4) * 32) >> 4);
           const uint32_t ka = kb + (((kk / 4) * kKChunk + (kk % 4) * 32) >> 4);
           if (kk == 0)
@@ -362,8 +368,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
         if (!wait_or_fail(L::bQFull, q_uses & 1)) break;
         ++q_uses;
         ptx::tc_fence_after();
-        // prologue: S(0), S(1)
-        for (int j = 0; ok && j < 2 && j < w.n; ++j) {
+        // prologue: S(0) .. S(NSB-1)
+        for (int j = 0; ok && j < NSB && j < w.n; ++j) {
           ok = wait_item(2u * j);
           if (!ok) break;
           issue_s(j, slot_of(2u * j));
@@ -372,7 +378,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
           if (j == w.n - 1) commit(L::bQEmpty);
         }
         for (int j = 0; ok && j < w.n; ++j) {
-          const int b = j & 1;
+          const int b = j % NSB;
           if (!wait_item(2u * j + 1u)) { ok = false; break; }
           if (!wait_or_fail(L::bPFull + b, pf_cnt[b] & 1)) { ok = false; break; }
           ++pf_cnt[b];
@@ -382,17 +388,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
           }
           ptx::tc_fence_after();
           issue_pv(b, slot_of(2u * j + 1u), j > 0);
-          commit(L::bPVDone);
+          commit(L::bPVDone + b);
           commit(L::bKVEmpty + (int)slot_of(2u * j + 1u));
           if (j == w.n - 1) commit(L::bODone);
-          // S(j+2) overwrites the buffer PV(j) reads P from; the pair's
+          // S(j+NSB) overwrites the buffer PV(j) reads P from; the pair's
           // tensor pipe runs MMAs in issue order, so it may follow at once.
-          if (j + 2 < w.n) {
-            if (!wait_item(2u * (j + 2))) { ok = false; break; }
-            issue_s(b, slot_of(2u * (j + 2)));
+          if (j + NSB < w.n) {
+            if (!wait_item(2u * (j + NSB))) { ok = false; break; }
+            issue_s(b, slot_of(2u * (j + NSB)));
             commit(L::bSFull + b);
-            commit(L::bKVEmpty + (int)slot_of(2u * (j + 2)));
-            if (j + 2 == w.n - 1) commit(L::bQEmpty);
+            commit(L::bKVEmpty + (int)slot_of(2u * (j + NSB)));
+            if (j + NSB == w.n - 1) commit(L::bQEmpty);
           }
         }
         ++used;
@@ -409,9 +415,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float c = p.scale_log2;
-    int sf_cnt[2] = {0, 0};
+    int sf_cnt[NSB] = {};
+    int pv_cnt[NSB] = {};  // P V MMAs reading each buffer, issued so far
     int units_done = 0;
-    int pv_base = 0;  // pair P V MMAs of earlier units
     bool ok = true;
     auto wait_all = [&](int slot, uint32_t parity) -> bool {
       bool w_ok = ptx::mbar_wait_cluster(bar(slot), parity, abort_flag, tmo);
@@ -459,7 +465,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
       const int row = w.row0 + kBM * (int)rank + r;  // this thread's query row
       float m = -INFINITY, l = 0.f, lr = 0.f;
       for (int j = 0; j < w.n; ++j) {
-        const int b = j & 1;
+        const int b = j % NSB;
         if (!wait_all(L::bSFull + b, sf_cnt[b] & 1)) { ok = false; break; }
         ++sf_cnt[b];
         ptx::tc_fence_after();
@@ -515,13 +521,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
         }
         // A row that moved its reference scales its O rows, once the P V of
         // the previous tile (the last writer of O) has landed; no later P V
-        // runs before this warp reports P ready.
+        // runs before this warp reports P ready.  That PV's buffer barrier
+        // has at most it outstanding (the one before it on the buffer is
+        // older than S(j)), so its parity is unambiguous.
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!wait_all(L::bPVDone, (uint32_t)(pv_base + j - 1) & 1u)) { ok = false; break; }
+          const int pb = (j - 1) % NSB;
+          if (!wait_all(L::bPVDone + pb, (uint32_t)(pv_cnt[pb] - 1) & 1u)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t o_addr = tmem + lane_off + L::kColO;
 #pragma unroll 1
-          for (int ch = 0; ch < kD / 32; ++ch) {
+          for (int ch = 0; ch < D / 32; ++ch) {
             uint32_t u[32];
             ptx::tmem_ld32(o_addr + ch * 32, u);
             ptx::tmem_wait_ld();
@@ -533,7 +542,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_cluster(bar0(L::bPFull + b));
+        // rank 0 arrives on its own barrier (CTA scope); the peer's warps
+        // release across the cluster.
+        if (lane == 0) {
+          if (leader)
+            ptx::mbar_arrive(bar(L::bPFull + b));
+          else
+            ptx::mbar_arrive_cluster(bar0(L::bPFull + b));
+        }
+        ++pv_cnt[b];  // PV(j) may be issued from here on
         const float pt = ex2(fmaf(tmax, c, -m_use));
         const float pt16 = unpack2<BF16>(pack2<BF16>(pt, 0.f)).x;
         l = alpha * l + sum;
@@ -541,7 +558,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
         m = m_use;
       }
       if (!ok) break;
-      pv_base += w.n;
       // The epilogue must have read the previous unit's statistics.
       if (units_done > 0 && !wait_all(L::bStatsFree, (units_done - 1) & 1)) break;
       ++units_done;
@@ -585,10 +601,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
       const bool valid = row < p.S;
       const size_t grow = (size_t)w.bh * (size_t)p.S + (size_t)row;
       uint4* const orow = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.o) +
-                                                   grow * (size_t)(kD * 2));
+                                                   grow * (size_t)(D * 2));
       const uint32_t o_addr = tmem + lane_off + L::kColO;
 #pragma unroll 2
-      for (int ch = 0; ch < kD / 32; ++ch) {
+      for (int ch = 0; ch < D / 32; ++ch) {
         uint32_t u[32];
         ptx::tmem_ld32(o_addr + ch * 32, u);
         ptx::tmem_wait_ld();

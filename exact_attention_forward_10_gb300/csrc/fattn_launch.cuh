@@ -93,23 +93,33 @@ cudaError_t launch_fwd_fp8(const LaunchArgs& a) {
   return cudaGetLastError();
 }
 
-// Head dim 256: the CTA-pair kernel (clusters of two CTAs, one per SM).
-constexpr int kPairStages = 5;
+// The CTA-pair kernel (clusters of two CTAs, one per SM) for head dim 256:
+// two TMEM score buffers and a 5-item ring of 32 KB halves.
+template <int D>
+struct PairConfig;
+template <>
+struct PairConfig<256> {
+  static constexpr int NSB = 2;
+  static constexpr int NS = 5;
+};
+template <int D>
 struct PairShape {
-  static constexpr int kSmem = pair::PairLayout<kPairStages>::kSmemBytes;
+  using C = PairConfig<D>;
+  static constexpr int kSmem = pair::PairLayout<D, C::NSB, C::NS>::kSmemBytes;
   static constexpr int kThreads = pair::PairWarps::kThreads;
 };
 
-template <bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16>
 cudaError_t set_pair_attr() {
-  auto kern = &pair::fattn_fwd_pair_kernel<kPairStages, CAUSAL, BF16>;
+  using C = PairConfig<D>;
+  auto kern = &pair::fattn_fwd_pair_kernel<D, C::NSB, C::NS, CAUSAL, BF16>;
   static volatile bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64 || !attr_set[dev]) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PairShape::kSmem);
+                             PairShape<D>::kSmem);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set[dev] = true;
   }
@@ -117,26 +127,28 @@ cudaError_t set_pair_attr() {
 }
 
 // a.grid counts CTAs (twice the clusters).
-template <bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16>
 cudaError_t launch_fwd_pair(const LaunchArgs& a) {
-  cudaError_t e = set_pair_attr<CAUSAL, BF16>();
+  using C = PairConfig<D>;
+  cudaError_t e = set_pair_attr<D, CAUSAL, BF16>();
   if (e != cudaSuccess) return e;
-  pair::fattn_fwd_pair_kernel<kPairStages, CAUSAL, BF16>
-      <<<a.grid, PairShape::kThreads, PairShape::kSmem, a.stream>>>(*a.tm_q, *a.tm_k,
-                                                                     *a.tm_v, a.params);
+  pair::fattn_fwd_pair_kernel<D, C::NSB, C::NS, CAUSAL, BF16>
+      <<<a.grid, PairShape<D>::kThreads, PairShape<D>::kSmem, a.stream>>>(
+          *a.tm_q, *a.tm_k, *a.tm_v, a.params);
   return cudaGetLastError();
 }
 
 // Clusters of the pair kernel that fit on the current device at once (the
 // persistent grid must not exceed it: work is assigned to clusters
 // statically).  0 on error.
-template <bool CAUSAL, bool BF16>
+template <int D, bool CAUSAL, bool BF16>
 int pair_clusters_fit() {
-  if (set_pair_attr<CAUSAL, BF16>() != cudaSuccess) return 0;
+  using C = PairConfig<D>;
+  if (set_pair_attr<D, CAUSAL, BF16>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(PairShape::kThreads);
-  cfg.dynamicSmemBytes = PairShape::kSmem;
+  cfg.blockDim = dim3(PairShape<D>::kThreads);
+  cfg.dynamicSmemBytes = PairShape<D>::kSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -145,8 +157,9 @@ int pair_clusters_fit() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, &pair::fattn_fwd_pair_kernel<kPairStages, CAUSAL, BF16>,
-                                     &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(
+          &n, &pair::fattn_fwd_pair_kernel<D, C::NSB, C::NS, CAUSAL, BF16>, &cfg) !=
+      cudaSuccess) {
     cudaGetLastError();
     return 0;
   }
