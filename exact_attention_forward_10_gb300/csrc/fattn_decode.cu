@@ -1,6 +1,7 @@
 // Host-side planning for attention against a key/value cache: the query-count
-// buckets, warps and shared memory of the split kernel, and the dispatch to
-// the per-head-dim instantiation units.
+// buckets (one query: the CUDA-core split kernel; 2 to 16: the warp-level MMA
+// split kernel), warps and shared memory of the split kernel, and the
+// dispatch to the per-head-dim instantiation units.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -9,26 +10,17 @@
 
 namespace fattn {
 namespace decode {
-int sq_bucket(int Sq) { return Sq <= 1 ? 1 : Sq <= 4 ? 4 : 16; }
+int sq_bucket(int Sq) { return Sq <= 1 ? 1 : kMaxSq; }
 
 int warps_per_cta(int D, int Sq) {
-  const int b = sq_bucket(Sq);
-  if (D == 64) return b == 1 ? DecodeLayout<64, 1>::kWarps
-                     : b == 4 ? DecodeLayout<64, 4>::kWarps
-                              : DecodeLayout<64, 16>::kWarps;
-  return b == 1 ? DecodeLayout<128, 1>::kWarps
-       : b == 4 ? DecodeLayout<128, 4>::kWarps
-                : DecodeLayout<128, 16>::kWarps;
+  if (sq_bucket(Sq) == 1) return D == 64 ? DecodeLayout<64, 1>::kWarps : DecodeLayout<128, 1>::kWarps;
+  return D == 64 ? DecodeMmaLayout<64>::kWarps : DecodeMmaLayout<128>::kWarps;
 }
 
 int smem_bytes(int D, int Sq) {
-  const int b = sq_bucket(Sq);
-  if (D == 64) return b == 1 ? DecodeLayout<64, 1>::kSmemBytes
-                     : b == 4 ? DecodeLayout<64, 4>::kSmemBytes
-                              : DecodeLayout<64, 16>::kSmemBytes;
-  return b == 1 ? DecodeLayout<128, 1>::kSmemBytes
-       : b == 4 ? DecodeLayout<128, 4>::kSmemBytes
-                : DecodeLayout<128, 16>::kSmemBytes;
+  if (sq_bucket(Sq) == 1)
+    return D == 64 ? DecodeLayout<64, 1>::kSmemBytes : DecodeLayout<128, 1>::kSmemBytes;
+  return D == 64 ? DecodeMmaLayout<64>::kSmemBytes : DecodeMmaLayout<128>::kSmemBytes;
 }
 
 cudaError_t launch(int D, bool bf16, const DecodeLaunch& a) {

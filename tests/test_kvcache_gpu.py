@@ -33,7 +33,7 @@ EDGE_LENS = [0, 1, 31, 32, 33, 95, 257, 300]
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("Sq", [1, 2, 4, 5, 16])
+@pytest.mark.parametrize("Sq", [1, 2, 4, 5, 11, 16])
 def test_ragged_lengths(Sq, D, dtype, causal):
     x = attn_inputs.make_kvcache(len(EDGE_LENS), 3, Sq, 300, D, dtype,
                                  seed=2000 + Sq + D)
@@ -77,6 +77,16 @@ def test_many_short_heads_per_warp():
     x = attn_inputs.make_kvcache(64, 32, 1, 96, 64, "bf16", seed=2400,
                                  lens_range=(0, 96))
     check_kvcache(x, False, "B64 H32 short")
+
+
+@pytest.mark.parametrize("Sq,D", [(8, 128), (16, 64)])
+def test_many_short_heads_per_warp_multi_query(Sq, D):
+    """The same with several queries (the tensor-core split kernel): every
+    head switch inside a warp writes a record and reloads the query rows."""
+    x = attn_inputs.make_kvcache(48, 16, Sq, 80, D, "fp16", seed=2450 + Sq,
+                                 lens_range=(0, 80))
+    for causal in (False, True):
+        check_kvcache(x, causal, f"B48 H16 Sq{Sq} D{D} short causal={causal}")
 
 
 def test_one_long_head_over_every_warp():
