@@ -389,9 +389,11 @@ KERNEL_SOURCES = {
                   "fattn_fwd_d128.cu", "ptx.cuh", "fattn_status.h"],
     "fattn_pair": ["fattn_kernel_pair.cuh", "fattn_kernel.cuh", "fattn_launch.cuh",
                    "fattn_fwd_d256.cu", "ptx.cuh", "fattn_status.h"],
-    "fattn_decode": ["fattn_decode.cuh", "fattn_decode_launch.h",
-                     "fattn_decode_d64.cu", "fattn_decode_d128.cu", "ptx.cuh",
-                     "fattn_status.h"],
+    "fattn_fwd_fp8": ["fattn_kernel.cuh", "fattn_launch.cuh", "fattn_fwd_fp8.cu",
+                      "ptx.cuh", "fattn_status.h"],
+    "fattn_decode": ["fattn_decode.cuh", "fattn_decode_mma.cuh", "fattn_decode_launch.h",
+                     "fattn_decode.cu", "fattn_decode_d64.cu", "fattn_decode_d128.cu",
+                     "ptx.cuh", "fattn_status.h"],
 }
 
 
@@ -623,7 +625,8 @@ def run_fp8(args):
                          "peak_kind": (f"fp8 dense = 2 x the {peaks['source']} bf16 burst "
                                        "(nominal fp8/bf16 ratio 4.5/2.25)"),
                          "kernel": "fattn_fwd_kernel<D=128, non-causal, E4M3 in, bf16 out>",
-                         "traffic": None},
+                         "traffic": load_traffic(f"fattn_fwd_noncausal_e4m3_d128_s{S}",
+                                                 "fattn_fwd_fp8")},
             "cpu_baseline": cpu,
             "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": sum(h.numel() for h in host),
@@ -868,8 +871,8 @@ def run_kvcache(args, w):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak["gbs"],
                          "unit": "GB/s", "frac": achieved / peak["gbs"],
                          "peak_kind": f"HBM copy, {peak['source']}",
-                         "kernel": "fattn_decode_kernel + merge (one call, both "
-                                   "launches inside the timed span)",
+                         "kernel": ("fattn_decode_kernel" if w.Sq == 1 else "fattn_decode_mma_kernel")
+                                   + " + merge (one call, both launches inside the timed span)",
                          "traffic": load_traffic(f"fattn_decode_{w.dtype}_d{w.D}_sq{w.Sq}_"
                                                  f"{args.kvcache}", "fattn_decode")},
             "cpu_baseline": cpu,
