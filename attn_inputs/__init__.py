@@ -141,6 +141,25 @@ def make_qkv(B: int, H: int, S: int, D: int, dtype: str, seed: int,
     return QKV(q=q, k=k, v=v, dtype=dtype, seed=seed, qk_mult=qk_mult)
 
 
+def make_qkv_shard(B_global: int, b0: int, b1: int, H: int, S: int, D: int,
+                   dtype: str, seed: int) -> QKV:
+    """Batch rows ``b0 .. b1-1`` of ``make_qkv(B_global, H, S, D, dtype,
+    seed)``, generated directly (the generator is counter-based: each row is
+    read at its own offset of the stream), so one rank of a data-parallel
+    run holds only its shard."""
+    if dtype not in DTYPES:
+        raise ValueError(f"unknown dtype {dtype!r}")
+    if not 0 <= b0 <= b1 <= B_global:
+        raise ValueError("shard outside the global batch")
+    per = H * S * D
+    n = B_global * per
+    shape = (b1 - b0, H, S, D)
+    q = gaussian_tensor(seed, b0 * per, shape, dtype)
+    k = gaussian_tensor(seed, n + b0 * per, shape, dtype)
+    v = gaussian_tensor(seed, 2 * n + b0 * per, shape, dtype)
+    return QKV(q=q, k=k, v=v, dtype=dtype, seed=seed, qk_mult=1.0)
+
+
 # --------------------------------------------------------------------------
 # The workloads: sizes, dtypes, masks and seeds of the benchmark shapes.
 # --------------------------------------------------------------------------

@@ -7,8 +7,10 @@ outputs are larger than L2, so no flush is needed between steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
-N > 1 runs under torchrun: every rank runs the same per-GPU workload (weak
-scaling, no collective on the data path); the timing is the max over ranks.
+N > 1 runs under torchrun as data parallelism over the batch (weak scaling):
+the global batch is N x 2 rows, each rank generates and runs its own shard of
+2 rows (no collective on the data path); the timing is the max over ranks.
+``--fp8`` and ``--kvcache`` run the same workload on every rank (replicas).
 ``--impl reference`` times the fp64 CPU oracle on a bounded row sample of the
 same workload (the reference arm: this path has no other implementation).
 
@@ -226,10 +228,15 @@ def run_fattn(args):
     dev = torch.device("cuda", torch.cuda.current_device())
     w = WORKLOAD
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
-    x = w.inputs()
+    # weak scaling: a global batch of world x B rows, each rank its own shard
+    from exact_attention_forward_10_gb300 import shard
+    global_b = world * w.B
+    b0, b1 = shard.batch_range(global_b, world, rank)
+    x = (w.inputs() if world == 1 else
+         attn_inputs.make_qkv_shard(global_b, b0, b1, w.H, w.S, w.D, w.dtype, w.seed))
     host = [torch.from_numpy(a).to(tdt).pin_memory() for a in (x.q, x.k, x.v)]
     q, k, v = (h.to(dev) for h in host)
-    B, H, S, D = w.B, w.H, w.S, w.D
+    B, H, S, D = b1 - b0, w.H, w.S, w.D
     outs = {c: (torch.empty_like(q), torch.empty((B, H, S), dtype=torch.float32, device=dev))
             for c in MASKS}
     stream = torch.cuda.Stream(dev)
@@ -322,12 +329,7 @@ def run_fattn(args):
               for o, l in h_outs.values())
 
     # ---- max over ranks
-    step_ms = elapsed_ms / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([step_ms, e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, e2e_ms = float(t[0]), float(t[1])
+    step_ms, e2e_ms = shard.max_over_ranks([elapsed_ms / args.steps, e2e_ms], device=dev)
 
     flops_step = sum(metric_flops(B, H, S, D, c) for c in MASKS)
     value = world * flops_step / (step_ms * 1e-3) / 1e12
@@ -356,7 +358,10 @@ def run_fattn(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
-            "config": workload_config(w, {"parallelism": f"replicas x{world}",
+            "config": workload_config(w, {"parallelism": (f"data parallel x{world}: each rank "
+                                                          f"{B} of {global_b} batch rows")
+                                                          if world > 1 else "one GPU",
+                                          "global_batch": global_b,
                                           "grid": plan["grid"], "block": plan["block"],
                                           "units_per_launch": plan["units"]}),
             "per_mask": per_mask,
