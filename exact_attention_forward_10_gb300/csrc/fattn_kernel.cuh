@@ -49,7 +49,8 @@
 #endif
 
 // Roles whose barrier waits spin instead of suspending (bit 0: load warp,
-// bit 1: MMA warp); a build-time choice.
+// bit 1: MMA warp, bit 2: softmax warps waiting for scores); a build-time
+// choice.
 #ifndef FATTN_SPIN_ROLES
 #define FATTN_SPIN_ROLES 0
 #endif
@@ -58,6 +59,7 @@ namespace fattn {
 
 constexpr bool kSpinLoad = (FATTN_SPIN_ROLES & 1) != 0;
 constexpr bool kSpinMma = (FATTN_SPIN_ROLES & 2) != 0;
+constexpr bool kSpinSoftmax = (FATTN_SPIN_ROLES & 4) != 0;
 constexpr int kBM = 128;  // query rows per tile (one TMEM lane each)
 constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kSwizzleChunkCols = 64;           // 128 bytes of 16-bit values
@@ -744,7 +746,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       bool ok = true;
       for (int j = 0; j < nk; ++j) {
         FATTN_TRACE_EV(k, j, 8 * i + 0);
-        ok = ptx::mbar_wait(bar(L::bSFull + i), sf_cnt & 1, abort_flag, tmo);
+        ok = ptx::mbar_wait<kSpinSoftmax>(bar(L::bSFull + i), sf_cnt & 1, abort_flag, tmo);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
           if (lane == 0) raise_error(p, abort_flag, kErrPipelineTimeout, kRoleSoftmax, L::bSFull + i);
