@@ -48,6 +48,16 @@
 #define FATTN_TRACE_EV(round, kv_tile, event) ((void)0)
 #endif
 
+// P V issued in two halves of the keys (the first half while the softmax
+// still works on the second) for 8-bit inputs, where P overwrites S; a
+// build-time choice (1: on).  Measured on the B2 H16 S8192 D128 workloads:
+// E4M3 1436 / 1367 TF against 1292 / 1247 in whole rows (the softmax is
+// longer and P V shorter than with 16-bit inputs); bf16 1335 / 1278 against
+// 1491 / 1412, so 16-bit inputs keep whole rows.
+#ifndef FATTN_HALF_PV
+#define FATTN_HALF_PV 1
+#endif
+
 // Roles whose barrier waits spin instead of suspending (bit 0: load warp,
 // bit 1: MMA warp, bit 2: softmax warps waiting for scores); a build-time
 // choice.
@@ -108,7 +118,9 @@ struct FwdLayout {
   static constexpr int bPVDone = bStats + QT;
   static constexpr int bOEmpty = bPVDone + QT;
   static constexpr int bDrain = bOEmpty + QT;
-  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int bP1Full = bDrain + 1;         // first half of P_i ready
+  static constexpr int bPV1Done = bP1Full + QT;      // its P V done
+  static constexpr int kNumBars = bPV1Done + QT;
   static constexpr int kMisc = kBars + kNumBars * 8;   // tmem base, abort flag
   static constexpr int kRowL = kMisc + 16;             // float [QT][128]
   static constexpr int kRowM = kRowL + QT * kBM * 4;   // float [QT][128]: LSE
@@ -120,6 +132,8 @@ struct FwdLayout {
   // S_i(j+1) can be computed while the softmax of tile j still runs; else P_i
   // overwrites the first 64 columns of S_i.
   static constexpr bool kSepP = QT * (128 + 64) + QT * D <= (int)kTmemCols;
+  // P over S with 8-bit inputs: P V in two halves of the keys (FATTN_HALF_PV)
+  static constexpr bool kHalfPV = FATTN_HALF_PV != 0 && !kSepP && EB == 1;
   __host__ __device__ static constexpr uint32_t colS(int i) { return 128u * i; }
   __host__ __device__ static constexpr uint32_t colP(int i) {
     return kSepP ? 128u * QT + 64u * i : colS(i);
@@ -147,6 +161,13 @@ struct FwdWarps {
   static_assert(QT != 2 || 2 * kRegSoftmax + kRegCorrection + kRegOther ==
                                4 * (65536 / kThreads),
                 "register split must equal the launch allocation");
+};
+
+// Keys [kFirst, kFirst + kCount) of a score row (an exponent pass over them).
+template <int FIRST, int COUNT>
+struct KeyRange {
+  static constexpr int kFirst = FIRST;
+  static constexpr int kCount = COUNT;
 };
 
 struct Unit {
@@ -318,6 +339,8 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       ptx::mbar_init(bar(L::bStats + i), kBM);
       ptx::mbar_init(bar(L::bPVDone + i), 1);
       ptx::mbar_init(bar(L::bOEmpty + i), kBM);
+      ptx::mbar_init(bar(L::bP1Full + i), kBM);
+      ptx::mbar_init(bar(L::bPV1Done + i), 1);
     }
     for (int s = 0; s < NS; ++s) {
       ptx::mbar_init(bar(L::bKVFull + s), 1);
@@ -472,13 +495,18 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       // O_i += P_i V: M = 128, N = D, K = 128 keys in steps of kK.  P_i is
       // read from TMEM (two 16-bit or four 8-bit values per column: 8
       // columns per step); V is MN-major, each step kK key rows further.
-      auto issue_pv = [&](int i, uint32_t v_slot, bool acc) {
+      // part: 0 all keys, 1 the first half, 2 the second half (accumulating).
+      auto issue_pv = [&](int i, uint32_t v_slot, bool acc, int part = 0) {
+        constexpr int kSteps = kBN / L::kK;
         const uint32_t d = tmem + L::colO(i);
         const uint32_t a = tmem + L::colP(i);
         const uint32_t vb = v_lo + v_slot * kTileLo;
         if (!ptx::elect_one()) return;
+        const int k0 = part == 2 ? kSteps / 2 : 0;
+        const int k1 = part == 1 ? kSteps / 2 : kSteps;
 #pragma unroll
-        for (int kk = 0; kk < kBN / L::kK; ++kk) {
+        for (int kk = 0; kk < kSteps; ++kk) {
+          if (kk < k0 || kk >= k1) continue;
           if (kk == 0)
             ptx::mma_ts_lohi<0, FP8>(d, a, vb, kHi, kIdPV, acc ? 1u : 0u);
           else
@@ -605,10 +633,23 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
             for (int i = 0; ok && i < QT; ++i) {
               if (j < n[i]) {
                 if (i == QT - 1) FATTN_TRACE_EV(k, j, 29);
+                if constexpr (L::kHalfPV) {
+                  // the first half of P is ready while the softmax still
+                  // works on the second: its P V goes first
+                  ok = wait_or_fail(L::bP1Full + i, p_cnt[i] & 1);
+                  if (ok && j == 0 && used[i] > 0) {
+                    ok = wait_or_fail(L::bOEmpty + i, oe_cnt[i] & 1);
+                    ++oe_cnt[i];
+                  }
+                  if (!ok) break;
+                  ptx::tc_fence_after();
+                  issue_pv(i, v_slot, j > 0, 1);
+                  commit(L::bPV1Done + i);
+                }
                 ok = wait_or_fail(L::bPFull + i, p_cnt[i] & 1);
                 ++p_cnt[i];
                 if (i == QT - 1) FATTN_TRACE_EV(k, j, 30);
-                if (ok && j == 0 && used[i] > 0) {
+                if (!L::kHalfPV && ok && j == 0 && used[i] > 0) {
                   ok = wait_or_fail(L::bOEmpty + i, oe_cnt[i] & 1);
                   ++oe_cnt[i];
                 }
@@ -616,7 +657,10 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                 if (i == QT - 1) FATTN_TRACE_EV(k, j, 31);
                 FATTN_TRACE_EV(k, j, 25 + 2 * i);
                 ptx::tc_fence_after();
-                issue_pv(i, v_slot, j > 0);
+                if constexpr (L::kHalfPV)
+                  issue_pv(i, v_slot, true, 2);
+                else
+                  issue_pv(i, v_slot, j > 0);
                 commit(L::bPVDone + i);
                 if (i == last_pv) commit(L::bKVEmpty + v_slot);
               }
@@ -656,15 +700,46 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
     int sf_cnt = 0;
     int units_done = 0;  // units of this tile whose row statistics were published
     int p_writes = 0;    // P_i buffer fills so far (separate-P layout)
+    int h1_published = 0;  // first halves of P_i published (half-P V layout)
+    // O_i rows of this warp's lane quarter times a (per row).  In the
+    // half-P V layout it may run while half a score row is still in
+    // registers: 16 columns at a time there.
+    auto rescale_o = [&](float a) {
+      const uint32_t o_addr = tmem + ((uint32_t)(quarter * 32) << 16) + L::colO(i);
+      if constexpr (L::kHalfPV) {
+#pragma unroll 1
+        for (int ch = 0; ch < D / 16; ++ch) {
+          uint32_t u[16];
+          ptx::tmem_ld16(o_addr + ch * 16, u);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * a);
+          ptx::tmem_st16(o_addr + ch * 16, u);
+        }
+      } else {
+#pragma unroll
+        for (int ch = 0; ch < D / 32; ++ch) {
+          uint32_t u[32];
+          ptx::tmem_ld32(o_addr + ch * 32, u);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * a);
+          ptx::tmem_st32(o_addr + ch * 32, u);
+        }
+      }
+    };
     // p = exp2(s*c - mref) for the row, with the scale folded into one packed
     // FFMA per pair; 16-bit P goes to TMEM over the S columns (the whole row
     // is in registers), the row sum runs in four packed partial sums, and
     // with TRACK the row maximum of s is taken on the side.
     // With FP8 also the sum of the weights as rounded to E4M3 (rsum): the
     // normaliser of O, so that O is exactly a convex combination of V rows.
+    // range_c: the keys (KeyRange); P of key kFirst goes to column addr.
     auto exp_pass = [&](const float (&s)[kBN], float mref, uint32_t addr, auto track_c,
-                        float& tmax, float& rsum) -> float {
+                        float& tmax, float& rsum, auto range_c) -> float {
       constexpr bool kTrack = decltype(track_c)::value;
+      constexpr int kFirst = decltype(range_c)::kFirst;
+      constexpr int kN = decltype(range_c)::kCount;
       const float2 c2 = make_float2(c, c);
       const float2 neg2 = make_float2(-mref, -mref);
       float2 sum2[4];
@@ -673,14 +748,14 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       for (int a = 0; a < 4; ++a) sum2[a] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int a = 0; a < 8; ++a) acc[a] = -INFINITY;
-      float r0 = 0.f, r1 = 0.f;
+      [[maybe_unused]] float r0 = 0.f, r1 = 0.f;
 #pragma unroll
-      for (int ch = 0; ch < kBN / 32; ++ch) {
+      for (int ch = 0; ch < kN / 32; ++ch) {
         uint32_t pk[16];
         float2 prev = make_float2(0.f, 0.f);
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float s0 = s[ch * 32 + 2 * e], s1 = s[ch * 32 + 2 * e + 1];
+          const float s0 = s[kFirst + ch * 32 + 2 * e], s1 = s[kFirst + ch * 32 + 2 * e + 1];
           if (kTrack) acc[e & 7] = fmax3(acc[e & 7], s0, s1);
           const float2 x = __ffma2_rn(make_float2(s0, s1), c2, neg2);
           const float2 pp = make_float2(ex2(x.x), ex2(x.y));
@@ -822,6 +897,103 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
             for (int e = 0; e < 16; ++e) part[e] = pk[ch * 16 + e];
             ptx::tmem_st16(p_addr + ch * 16, part);
           }
+        } else if constexpr (L::kHalfPV) {
+          // P V in two halves of the keys.  The first tile of a row takes
+          // its maximum first; later tiles exponentiate each half against
+          // the current reference with the maximum on the side, and a half
+          // whose maximum passed the reference by more than kRescaleLog2
+          // moves it and is redone (warp-uniformly).  The first half's P is
+          // published before the second is computed; if the second half
+          // moves the reference, O (which then holds the first half's P V)
+          // is rescaled once that P V has landed, with l and lr: the same
+          // result, since alpha * p_old = p_new.
+          if (j == 0) {
+            float acc[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) acc[a] = fmax3(s[2 * a], s[2 * a + 1], -INFINITY);
+#pragma unroll
+            for (int e = 16; e < kBN; e += 16) {
+#pragma unroll
+              for (int a = 0; a < 8; ++a) acc[a] = fmax3(acc[a], s[e + 2 * a], s[e + 2 * a + 1]);
+            }
+            m_use = c * fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
+                              fmaxf(acc[6], acc[7]));
+            if (m_use == -INFINITY) m_use = 0.f;  // no allowed key in this row
+          }
+          FATTN_TRACE_EV(k, j, 8 * i + 3);
+          constexpr int kHalf = kBN / 2;
+          constexpr uint32_t kPHalfCols = FP8 ? kHalf / 4 : kHalf / 2;
+          // the largest weight of a half as the MMA sees it, minus its fp32 value
+          auto round_corr = [&](float tm, float mr) -> float {
+            if constexpr (FP8) {
+              return 0.f;
+            } else {
+              const float pt = ex2(fmaf(tm, c, -mr));
+              return unpack2<BF16>(pack2<BF16>(pt, 0.f)).x - pt;
+            }
+          };
+          // ---- first half
+          float tmax0 = -INFINITY, rsum0 = 0.f;
+          float sum0 = exp_pass(s, m_use, s_addr, std::true_type{}, tmax0, rsum0,
+                                KeyRange<0, kHalf>{});
+          if (j > 0) {
+            const float mxc = tmax0 * c;
+            const bool move = mxc > m + kRescaleLog2;
+            if (__any_sync(0xffffffffu, move)) {
+              if (move) {
+                m_use = mxc;
+                alpha = ex2(m - m_use);
+              }
+              sum0 = exp_pass(s, m_use, s_addr, std::false_type{}, tmax0, rsum0,
+                              KeyRange<0, kHalf>{});
+            }
+          }
+          // PV_i(j-1) has landed (S_i(j) was issued after it): O may change
+          if (__any_sync(0xffffffffu, alpha != 1.f)) rescale_o(alpha);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::bP1Full + i));
+          ++h1_published;
+          l = alpha * l + sum0;
+          lr = alpha * lr + (FP8 ? rsum0 : sum0 + round_corr(tmax0, m_use));
+          m = m_use;
+          // ---- second half
+          float tmax1 = -INFINITY, rsum1 = 0.f;
+          float sum1 = exp_pass(s, m, s_addr + kPHalfCols, std::true_type{}, tmax1, rsum1,
+                                KeyRange<kHalf, kHalf>{});
+          {
+            const float mxc = tmax1 * c;
+            const bool move = mxc > m + kRescaleLog2;
+            if (__any_sync(0xffffffffu, move)) {
+              float m_new = m, alpha1 = 1.f;
+              if (move) {
+                m_new = mxc;
+                alpha1 = ex2(m - m_new);
+              }
+              sum1 = exp_pass(s, m_new, s_addr + kPHalfCols, std::false_type{}, tmax1, rsum1,
+                              KeyRange<kHalf, kHalf>{});
+              // the first half's P V must have landed before O is rescaled
+              bool w_ok = ptx::mbar_wait(bar(L::bPV1Done + i), (uint32_t)(h1_published - 1) & 1u,
+                                         abort_flag, tmo);
+              w_ok = __all_sync(0xffffffffu, w_ok);
+              if (!w_ok) {
+                if (lane == 0) raise_error(p, abort_flag, kErrPipelineTimeout, kRoleSoftmax, L::bPV1Done + i);
+                ok = false;
+                break;
+              }
+              ptx::tc_fence_after();
+              if (__any_sync(0xffffffffu, alpha1 != 1.f)) rescale_o(alpha1);
+              l *= alpha1;
+              lr *= alpha1;
+              m = m_new;
+            }
+          }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar(L::bPFull + i));
+          FATTN_TRACE_EV(k, j, 8 * i + 4);
+          l += sum1;
+          lr += FP8 ? rsum1 : sum1 + round_corr(tmax1, m);
         } else {
           // Reference maximum m (log2 domain).  The first tile of a row has
           // none yet: take its maximum first.  Later tiles exponentiate against
@@ -845,7 +1017,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           }
           FATTN_TRACE_EV(k, j, 8 * i + 3);
           tmax = -INFINITY;
-          sum = exp_pass(s, m_use, s_addr, std::true_type{}, tmax, rsum);
+          sum = exp_pass(s, m_use, s_addr, std::true_type{}, tmax, rsum, KeyRange<0, kBN>{});
           if (j > 0) {
             const float mxc = tmax * c;
             const bool move = mxc > m + kRescaleLog2;
@@ -854,27 +1026,17 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                 m_use = mxc;
                 alpha = ex2(m - m_use);
               }
-              sum = exp_pass(s, m_use, s_addr, std::false_type{}, tmax, rsum);
+              sum = exp_pass(s, m_use, s_addr, std::false_type{}, tmax, rsum, KeyRange<0, kBN>{});
             }
           }
         }
+        if constexpr (!L::kHalfPV) {
         // A row that moved its reference scales its O by exp2(m_old - m_new).
         // This warp owns these O rows (its TMEM lane quarter) and may touch
         // them now: PV_i(j-1) has landed (with P aliasing S, S_i(j) was
         // issued after it; with separate P, its completion was awaited
         // above), and no MMA writes O_i until this warp reports P ready.
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const uint32_t o_addr = tmem + ((uint32_t)(quarter * 32) << 16) + L::colO(i);
-#pragma unroll
-          for (int ch = 0; ch < D / 32; ++ch) {
-            uint32_t u[32];
-            ptx::tmem_ld32(o_addr + ch * 32, u);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-            ptx::tmem_st32(o_addr + ch * 32, u);
-          }
-        }
+        if (__any_sync(0xffffffffu, alpha != 1.f)) rescale_o(alpha);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar(L::bPFull + i));
@@ -893,6 +1055,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           lr = alpha * lr + (sum + (pt16 - pt));
         }
         m = m_use;
+        }
       }
       if (!ok) break;
       // The previous unit's epilogue must have read its statistics before
