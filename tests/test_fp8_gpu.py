@@ -64,6 +64,26 @@ def test_large_scores():
         _check(o, lse, ro, rl, tol, f"fp8 x4 causal={causal}")
 
 
+@pytest.mark.parametrize("jstar", [100, 148, 228, 300])
+def test_reference_moves_inside_a_tile(jstar):
+    """Every query is one vector u and key j* is u too, so each row's score
+    jumps at key j* by ~16 log2 units (past the 8 a reference may lag): in
+    the first key tile (whose maximum is taken first), in the first half of
+    a later tile, and in its second half, where O already holds the first
+    half's P V and is rescaled after it."""
+    x = attn_inputs.make_qkv_fp8(1, 2, 384, 128, seed=6600)
+    _, ks, _ = x.descale
+    x.q8[:] = x.q8[0, 0, 0]
+    x.q[:] = x.q[0, 0, 0]
+    codes = attn_inputs.e4m3_encode(x.q[0, 0, 0] / ks)
+    x.k8[:, :, jstar] = codes
+    x.k[:, :, jstar] = attn_inputs.e4m3_decode(codes) * ks
+    for causal in (False, True):
+        o, lse = run_cuda_fp8(x, causal, SCALE)
+        ro, rl, tol = fp8_bound(x, causal, SCALE)
+        _check(o, lse, ro, rl, tol, f"fp8 jump at key {jstar} causal={causal}")
+
+
 @pytest.mark.parametrize("causal", [False, True])
 def test_zero_queries_give_exact_means(causal):
     """Q = 0: every weight is exactly 1 (exact in E4M3), so O is the mean of

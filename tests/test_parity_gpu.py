@@ -94,6 +94,19 @@ def test_sweep_sampled(w):
                       stride=64, n_heads=2)
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("jstar", [100, 148, 228, 300])
+def test_reference_moves_inside_a_tile(jstar, dtype):
+    """Every query is one vector u and key j* is u too: each row's scaled
+    score jumps at key j* by ~16 log2 units, past the 8 a reference may lag,
+    in the first key tile, in the first or the second half of a later one."""
+    x = attn_inputs.make_qkv(1, 2, 384, 128, dtype, seed=6700)
+    x.q[:] = x.q[0, 0, 0]
+    x.k[:, :, jstar] = x.q[0, 0, 0]
+    for causal in (False, True):
+        check_full(x, causal, f"jump at key {jstar} {dtype} causal={causal}")
+
+
 def test_many_heads_short_sequences():
     x = attn_inputs.make_qkv(8, 64, 256, 64, "fp16", seed=11)
     for causal in (False, True):
