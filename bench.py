@@ -142,6 +142,58 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def pipelined_e2e_ms(torch, dev, stream, host, launch_into, new_outputs, h_outs, steps,
+                     barrier) -> float:
+    """Milliseconds per step of a stream of end-to-end steps: each copies its
+    inputs (``host``, pinned) to the GPU, runs ``launch_into(inputs,
+    outputs)`` on ``stream`` and copies the outputs to ``h_outs`` (pinned;
+    mask -> (O, LSE)); step k+1's input copy and step k-1's output copy
+    overlap step k's kernels (an H2D and a D2H stream, two device buffers,
+    events between them)."""
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    din = [[torch.empty_like(h, device=dev) for h in host] for _ in range(2)]
+    dout = [new_outputs() for _ in range(2)]
+    ev_in, ev_done, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+    def run(n):
+        for kstep in range(n):
+            b = kstep % 2
+            if kstep >= 2:
+                h2d_s.wait_event(ev_done[b])  # step k-2's kernels have read din[b]
+            with torch.cuda.stream(h2d_s):
+                for dst, src in zip(din[b], host):
+                    dst.copy_(src, non_blocking=True)
+                ev_in[b].record(h2d_s)
+            stream.wait_event(ev_in[b])
+            if kstep >= 2:
+                stream.wait_event(ev_out[b])  # step k-2's outputs are on the host
+            with torch.cuda.stream(stream):
+                launch_into(din[b], dout[b])
+                ev_done[b].record(stream)
+            d2h_s.wait_event(ev_done[b])
+            with torch.cuda.stream(d2h_s):
+                for c, (ho, hl) in h_outs.items():
+                    ho.copy_(dout[b][c][0], non_blocking=True)
+                    hl.copy_(dout[b][c][1], non_blocking=True)
+                ev_out[b].record(d2h_s)
+
+    run(2)
+    barrier()
+    p0 = torch.cuda.Event(enable_timing=True)
+    p1 = torch.cuda.Event(enable_timing=True)
+    p0.record(h2d_s)
+    stream.wait_event(p0)
+    d2h_s.wait_event(p0)
+    run(steps)
+    p1.record(d2h_s)
+    barrier()
+    return p0.elapsed_time(p1) / steps
+
+
+E2E_SCHEDULE = ("steps pipelined: step k+1's H2D and step k-1's D2H overlap step k's "
+                "kernels (three streams, two buffers)")
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -330,48 +382,12 @@ def run_fattn(args):
     barrier()
     e2e_serial_ms = e0.elapsed_time(e1) / e2e_steps
 
-    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    din = [[torch.empty_like(q) for _ in range(3)] for _ in range(2)]
-    dout = [{c: (torch.empty_like(q), torch.empty((B, H, S), dtype=torch.float32, device=dev))
-             for c in MASKS} for _ in range(2)]
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_done = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
-
-    def e2e_pipelined(n):
-        for kstep in range(n):
-            b = kstep % 2
-            if kstep >= 2:
-                h2d_s.wait_event(ev_done[b])  # step k-2's kernels have read din[b]
-            with torch.cuda.stream(h2d_s):
-                for dst, src in zip(din[b], host):
-                    dst.copy_(src, non_blocking=True)
-                ev_in[b].record(h2d_s)
-            stream.wait_event(ev_in[b])
-            if kstep >= 2:
-                stream.wait_event(ev_out[b])  # step k-2's outputs are on the host
-            with torch.cuda.stream(stream):
-                for c in MASKS:
-                    launch(c, *din[b], into=dout[b])
-                ev_done[b].record(stream)
-            d2h_s.wait_event(ev_done[b])
-            with torch.cuda.stream(d2h_s):
-                for c in MASKS:
-                    h_outs[c][0].copy_(dout[b][c][0], non_blocking=True)
-                    h_outs[c][1].copy_(dout[b][c][1], non_blocking=True)
-                ev_out[b].record(d2h_s)
-
-    e2e_pipelined(2)
-    barrier()
-    p0 = torch.cuda.Event(enable_timing=True)
-    p1 = torch.cuda.Event(enable_timing=True)
-    p0.record(h2d_s)
-    stream.wait_event(p0)
-    d2h_s.wait_event(p0)
-    e2e_pipelined(e2e_steps)
-    p1.record(d2h_s)
-    barrier()
-    e2e_ms = p0.elapsed_time(p1) / e2e_steps
+    e2e_ms = pipelined_e2e_ms(
+        torch, dev, stream, host,
+        lambda din, dout: [launch(c, *din, into=dout) for c in MASKS],
+        lambda: {c: (torch.empty_like(q), torch.empty((B, H, S), dtype=torch.float32, device=dev))
+                 for c in MASKS},
+        h_outs, e2e_steps, barrier)
     h2d = sum(h.numel() * h.element_size() for h in host)
     d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size()
               for o, l in h_outs.values())
@@ -425,8 +441,7 @@ def run_fattn(args):
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                    "schedule": ("steps pipelined: step k+1's H2D and step k-1's D2H "
-                                 "overlap step k's kernels (three streams, two buffers)"),
+                    "schedule": E2E_SCHEDULE,
                     "serial": {"value": world * flops_step / (e2e_serial_ms * 1e-3) / 1e12,
                                "ms_per_step": e2e_serial_ms}},
             "gpu_launches": args.steps * len(MASKS),
@@ -574,8 +589,8 @@ def run_fp8(args):
     sptr = stream.cuda_stream
     qs, ks, vs = x.descale
 
-    def launch(causal, qq, kk, vv):
-        o, l = outs[causal]
+    def launch(causal, qq, kk, vv, into=None):
+        o, l = (into or outs)[causal]
         rc = fattn.fattn_fwd_fp8(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
                                  l.data_ptr(), B, H, S, D, causal, w.scale, qs, ks, vs,
                                  fattn.FATTN_BF16, sptr)
@@ -648,12 +663,16 @@ def run_fp8(args):
             e2e_step()
         e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / n_e2e
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([step_ms, e2e_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, e2e_ms = float(t[0]), float(t[1])
+    e2e_serial_ms = e0.elapsed_time(e1) / n_e2e
+    e2e_ms = pipelined_e2e_ms(
+        torch, dev, stream, host,
+        lambda din, dout: [launch(c, *din, into=dout) for c in MASKS],
+        lambda: {c: (torch.empty((B, H, S, D), dtype=torch.bfloat16, device=dev),
+                     torch.empty((B, H, S), dtype=torch.float32, device=dev)) for c in MASKS},
+        h_outs, n_e2e, barrier)
+    from exact_attention_forward_10_gb300 import shard
+    step_ms, e2e_ms, e2e_serial_ms = shard.max_over_ranks([step_ms, e2e_ms, e2e_serial_ms],
+                                                          device=dev)
     flops_step = sum(metric_flops(B, H, S, D, c) for c in MASKS)
     peaks = load_peaks()
     peak8 = 2.0 * peaks["burst"]
@@ -690,7 +709,9 @@ def run_fp8(args):
                     "h2d_bytes_per_step": sum(h.numel() for h in host),
                     "d2h_bytes_per_step": sum(o.numel() * 2 + l.numel() * 4
                                               for o, l in h_outs.values()),
-                    "ms_per_step": e2e_ms},
+                    "ms_per_step": e2e_ms, "schedule": E2E_SCHEDULE,
+                    "serial": {"value": world * flops_step / (e2e_serial_ms * 1e-3) / 1e12,
+                               "ms_per_step": e2e_serial_ms}},
             "gpu_launches": args.steps * len(MASKS),
             "clocks": clocks}), flush=True)
     if world > 1:
