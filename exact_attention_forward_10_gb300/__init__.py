@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
         l.fattn_error_string.restype = ctypes.c_char_p
         l.fattn_plan.argtypes = [i, i, i, i, i, ip, ip, ip, ip, ip, ip]
         l.fattn_plan.restype = i
+        l.fattn_check_wait_timeout.argtypes = [i, vp]
+        l.fattn_check_wait_timeout.restype = i
         u64 = ctypes.c_ulonglong
         l.fattn_fwd_kvcache.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i,
                                         i, f, i, vp, u64, vp]
@@ -97,6 +99,13 @@ def fattn_last_error(stream=0):
 
 def fattn_error_string(status: int) -> str:
     return lib().fattn_error_string(status).decode()
+
+
+def fattn_check_wait_timeout(timeout_us: int, stream=None) -> int:
+    """Enqueue the bounded-wait check (a wait that nothing completes gives up
+    after ``timeout_us`` and records a pipeline timeout); read the outcome
+    with ``fattn_last_error``."""
+    return lib().fattn_check_wait_timeout(int(timeout_us), stream)
 
 
 def fattn_plan(B, H, S, D, causal=False) -> dict:

@@ -339,6 +339,26 @@ int fwd_grid(const Plan& plan, int D, bool causal, bool bf16, int sms) {
   return 2 * clusters;
 }
 
+// One warp waits on a shared-memory barrier that nothing completes, with the
+// bounded wait every kernel of the library uses: it must give up after
+// timeout_ns, record a pipeline timeout in the status block and return.
+__global__ void wait_check_kernel(int* status, unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t barrier_word;
+  __shared__ int abort_flag;
+  const uint32_t b = ptx::smem_u32(&barrier_word);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(b, 1);
+    abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncwarp();
+  const bool done = ptx::mbar_wait(b, 0, &abort_flag, timeout_ns);
+  if (!__any_sync(0xffffffffu, done) && threadIdx.x == 0 && atomicCAS(status, 0, kErrPipelineTimeout) == 0) {
+    status[1] = kRoleWaitCheck << 8;
+    status[2] = (int)blockIdx.x;
+  }
+}
+
 }  // namespace
 }  // namespace fattn
 
@@ -631,6 +651,17 @@ FATTN_API int fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o
     cudaGetLastError();
     return FATTN_ERR_LAUNCH;
   }
+  return FATTN_OK;
+}
+
+FATTN_API int fattn_check_wait_timeout(int timeout_us, fattn_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return FATTN_ERR_INVALID_ARG;
+  DeviceState* ds = nullptr;
+  const int rc = current_device(&ds, nullptr);
+  if (rc != kOk) return rc;
+  wait_check_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      ds->status, (unsigned long long)timeout_us * 1000ull);
+  if (cudaGetLastError() != cudaSuccess) return FATTN_ERR_LAUNCH;
   return FATTN_OK;
 }
 

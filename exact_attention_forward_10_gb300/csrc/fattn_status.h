@@ -22,5 +22,7 @@ constexpr int kStatusWords = 4;
 
 // Roles and barrier ids recorded in status word 1.
 enum Role : int { kRoleLoad = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleCorrection = 4 };
+// (5 and 6 are the cache kernels' roles.)  The bounded-wait check kernel:
+constexpr int kRoleWaitCheck = 7;
 
 }  // namespace fattn

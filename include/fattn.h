@@ -126,6 +126,18 @@ FATTN_API int fattn_fwd_fp8(const void *q, const void *k, const void *v, void *o
  */
 FATTN_API int fattn_last_error(fattn_stream_t stream, int *detail);
 
+/*
+ * Checks the device-side bounded wait the kernels use: one warp waits on a
+ * shared-memory barrier that nothing completes, with a limit of timeout_us
+ * microseconds (1 .. 1000000); it gives up, records
+ * FATTN_ERR_PIPELINE_TIMEOUT in the device status block (detail[0] = 7 << 8)
+ * and exits, leaving the context usable.  Enqueued on ``stream``; read the
+ * outcome with fattn_last_error.  Returns FATTN_OK once enqueued,
+ * FATTN_ERR_INVALID_ARG for a limit out of range, or the device errors of
+ * fattn_fwd.
+ */
+FATTN_API int fattn_check_wait_timeout(int timeout_us, fattn_stream_t stream);
+
 /* A static, human-readable string for a status code. */
 FATTN_API const char *fattn_error_string(int status);
 

@@ -153,3 +153,8 @@ def test_fp8_host_side_rejections(lib, args, want):
                              a["S"], a["D"], a["causal"], a["scale"], a["qs"], a["ks"],
                              a["vs"], a["out"], a["stream"])
     assert rc == want
+
+
+def test_wait_check_rejects_out_of_range_limits(lib):
+    for us in (0, -5, 1000001):
+        assert fattn.fattn_check_wait_timeout(us, 0) == fattn.FATTN_ERR_INVALID_ARG
