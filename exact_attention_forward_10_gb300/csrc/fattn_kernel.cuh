@@ -15,16 +15,22 @@
 //                  NS-stage mbarrier ring.
 //   * MMA warp:    one thread issues tcgen05.mma: S_i = Q_i K_j^T into TMEM
 //                  (fp32, 128 lanes x 128 columns), then O_i += P_i V_j with
-//                  P_i read from TMEM (16-bit, aliasing S_i) and O_i kept in
-//                  TMEM for the whole unit.
+//                  P_i read from TMEM and O_i kept in TMEM for the whole unit.
+//                  Head dim 128 (and 8-bit inputs): P_i overwrites S_i, the
+//                  two query tiles alternate (ping-pong).  Head dim 64: P_i
+//                  has its own columns, so scores run two key tiles ahead.
+//                  8-bit inputs: kind::f8f6f4 MMAs, P in E4M3, and P V in two
+//                  halves of the keys (the first half's MMAs overlap the
+//                  softmax of the second).
 //   * softmax warpgroup per query tile: thread r owns row r (TMEM lane r):
-//                  tcgen05.ld of its score row, mask, row max, exp2 with the
-//                  scale folded into one FFMA, row sum, 16-bit P back to TMEM.
+//                  tcgen05.ld of its score row, mask, exp2 against a lazily
+//                  moved reference maximum with the scale folded into one
+//                  FFMA, row sums, P back to TMEM; when a row's reference
+//                  moves, the same warp rescales that row of O_i in TMEM.
 //                  (m, l) live in registers; no shuffles are needed because a
 //                  row never leaves its thread.
-//   * correction warpgroup: rescales O_i in TMEM only when some row's max
-//                  moved (alpha != 1), and runs the epilogue: one 1/l per row,
-//                  cast to 16-bit, vector stores of O and the LSE.
+//   * epilogue warpgroup: one 1/l per row, cast to 16-bit, vector stores of
+//                  O and the LSE, while the next unit's tiles run.
 // Every wait is bounded; a timeout records an error in the device status
 // block and the CTA unwinds (frees TMEM, waits for its own copies) instead of
 // hanging.
