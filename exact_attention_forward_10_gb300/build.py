@@ -6,7 +6,7 @@ statically, so the library loads on machines without a GPU driver.
 
     python -m exact_attention_forward_10_gb300.build [--verbose]
 
-Extra nvcc flags (for experiments, e.g. -DFATTN_WAIT_SPIN=1) may be given in
+Extra nvcc flags (for experiments, e.g. -DFATTN_SPIN_ROLES=2) may be given in
 the FATTN_NVCC_FLAGS environment variable; they force a rebuild.
 """
 from __future__ import annotations

@@ -28,10 +28,12 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion,
                                    CUtensorMapFloatOOBfill);
 using AddressRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
 
 struct DriverFns {
   EncodeTiledFn encode = nullptr;
   AddressRangeFn range = nullptr;
+  CtxGetCurrentFn ctx_current = nullptr;
 };
 
 // Driver entry points through the runtime, so the library loads (and its
@@ -50,6 +52,11 @@ const DriverFns& driver() {
                                          cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
       f.range = reinterpret_cast<AddressRangeFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      f.ctx_current = reinterpret_cast<CtxGetCurrentFn>(p);
     cudaGetLastError();
     return f;
   }();
@@ -78,6 +85,22 @@ unsigned long long wait_timeout_ns() {
   return t;
 }
 
+// Make sure the calling thread has a current context.  The driver calls of
+// the buffer checks (cuMemGetAddressRange) need one, and a host thread that
+// has made no context-creating runtime call yet has none: there the current
+// device's primary context is bound to the thread (cudaSetDevice on the
+// device the thread already has, which changes nothing else).
+int bind_context(int dev) {
+  const DriverFns& f = driver();
+  CUcontext ctx = nullptr;
+  if (f.ctx_current && f.ctx_current(&ctx) == CUDA_SUCCESS && ctx) return kOk;
+  if (cudaSetDevice(dev) != cudaSuccess) {
+    cudaGetLastError();
+    return kErrCuda;
+  }
+  return kOk;
+}
+
 // The current device's state, created on first use (device query, status
 // block allocation).  Must not first run inside a stream capture.
 int current_device(DeviceState** out, int* dev_out) {
@@ -87,6 +110,7 @@ int current_device(DeviceState** out, int* dev_out) {
     return kErrUnsupported;
   }
   if (dev < 0 || dev >= kMaxDevices) return kErrUnsupported;
+  if (const int rc = bind_context(dev); rc != kOk) return rc;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState& d = g_dev[dev];
   if (!d.init) {
@@ -286,6 +310,7 @@ int noalloc_device(NoAllocState** out, int* dev_out) {
     return kErrUnsupported;
   }
   if (dev < 0 || dev >= kMaxDevices) return kErrUnsupported;
+  if (const int rc = bind_context(dev); rc != kOk) return rc;
   std::lock_guard<std::mutex> lock(g_mu);
   NoAllocState& d = g_noalloc[dev];
   if (!d.init) {
@@ -319,7 +344,7 @@ int noalloc_device(NoAllocState** out, int* dev_out) {
 
 // CTAs of the persistent grid: one per SM, but for the CTA-pair kernel (D =
 // 256) twice the clusters that fit at once (occupancy query, cached per
-// device and mask/dtype).
+// device and mask/dtype under the library mutex).
 int fwd_grid(const Plan& plan, int D, bool causal, bool bf16, int sms) {
   if (!use_pair(D)) return plan.total_units < sms ? plan.total_units : sms;
   static int fit[kMaxDevices][4] = {};
@@ -328,11 +353,13 @@ int fwd_grid(const Plan& plan, int D, bool causal, bool bf16, int sms) {
     cudaGetLastError();
     return 0;
   }
-  int* slot = dev < kMaxDevices ? &fit[dev][(causal ? 2 : 0) + (bf16 ? 1 : 0)] : nullptr;
-  int clusters = slot ? *slot : 0;
-  if (clusters <= 0) {
-    clusters = pair_clusters_d256(causal, bf16);
-    if (slot) *slot = clusters;
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  int clusters = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    int& slot = fit[dev][(causal ? 2 : 0) + (bf16 ? 1 : 0)];
+    if (slot <= 0) slot = pair_clusters_d256(causal, bf16);
+    clusters = slot;
   }
   if (clusters <= 0) return 0;
   if (plan.total_units < clusters) clusters = plan.total_units;
@@ -385,7 +412,6 @@ FATTN_API const char* fattn_error_string(int status) {
 FATTN_API int fattn_plan(int B, int H, int S, int D, int causal, int* grid,
                          int* block, int* smem_bytes, int* units,
                          int* q_tiles_per_unit, int* kv_stages) {
-  (void)causal;
   Plan plan;
   const int rc = host_checks(B, H, S, D, &plan);
   if (rc != kOk) return rc;

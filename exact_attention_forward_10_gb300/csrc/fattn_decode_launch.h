@@ -7,6 +7,7 @@
 
 #include "fattn_decode.cuh"
 #include "fattn_decode_mma.cuh"
+#include "fattn_smem_opt_in.h"
 
 namespace fattn {
 namespace decode {
@@ -55,16 +56,9 @@ template <int D, bool BF16>
 cudaError_t launch_split_mma(const DecodeLaunch& a) {
   using L = DecodeMmaLayout<D>;
   auto kern = &fattn_decode_mma_kernel<D, BF16>;
-  static volatile bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<bool> attr_set[64];
+  cudaError_t e = smem_opt_in(kern, L::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set[dev] = true;
-  }
   kern<<<a.grid, L::kThreads, L::kSmemBytes, a.stream>>>(*a.tm_k, *a.tm_v, a.params);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -75,16 +69,9 @@ template <int D, int SQ, bool BF16>
 cudaError_t launch_split(const DecodeLaunch& a) {
   using L = DecodeLayout<D, SQ>;
   auto kern = &fattn_decode_kernel<D, SQ, BF16>;
-  static volatile bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<bool> attr_set[64];
+  cudaError_t e = smem_opt_in(kern, L::kSmemBytes, attr_set);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             L::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set[dev] = true;
-  }
   kern<<<a.grid, L::kThreads, L::kSmemBytes, a.stream>>>(*a.tm_k, *a.tm_v, a.params);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

@@ -7,6 +7,7 @@
 
 #include "fattn_kernel.cuh"
 #include "fattn_kernel_pair.cuh"
+#include "fattn_smem_opt_in.h"
 
 namespace fattn {
 
@@ -49,18 +50,9 @@ cudaError_t launch_fwd(const LaunchArgs& a) {
   using C = FwdConfig<D>;
   auto kern = &fattn_fwd_kernel<D, C::QT, C::NS, CAUSAL, BF16>;
   constexpr int smem = FwdShape<D>::kSmem;
-  // The shared-memory opt-in is per function and device; remember it for the
-  // first 64 devices (setting it twice is harmless).
-  static volatile bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<bool> attr_set[64];
+  cudaError_t e = smem_opt_in(kern, smem, attr_set);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             smem);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set[dev] = true;
-  }
   kern<<<a.grid, FwdShape<D>::kThreads, smem, a.stream>>>(*a.tm_q, *a.tm_k,
                                                           *a.tm_v, a.params);
   return cudaGetLastError();
@@ -78,16 +70,9 @@ struct Fp8Shape {
 template <bool CAUSAL, bool BF16>
 cudaError_t launch_fwd_fp8(const LaunchArgs& a) {
   auto kern = &fattn_fwd_kernel<128, 2, kFp8Stages, CAUSAL, BF16, true>;
-  static volatile bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static std::atomic<bool> attr_set[64];
+  cudaError_t e = smem_opt_in(kern, Fp8Shape::kSmem, attr_set);
   if (e != cudaSuccess) return e;
-  if (dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Fp8Shape::kSmem);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set[dev] = true;
-  }
   kern<<<a.grid, Fp8Shape::kThreads, Fp8Shape::kSmem, a.stream>>>(*a.tm_q, *a.tm_k,
                                                                   *a.tm_v, a.params);
   return cudaGetLastError();
@@ -113,17 +98,8 @@ template <int D, bool CAUSAL, bool BF16>
 cudaError_t set_pair_attr() {
   using C = PairConfig<D>;
   auto kern = &pair::fattn_fwd_pair_kernel<D, C::NSB, C::NS, CAUSAL, BF16>;
-  static volatile bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PairShape<D>::kSmem);
-    if (e != cudaSuccess) return e;
-    if (dev < 64) attr_set[dev] = true;
-  }
-  return cudaSuccess;
+  static std::atomic<bool> attr_set[64];
+  return smem_opt_in(kern, PairShape<D>::kSmem, attr_set);
 }
 
 // a.grid counts CTAs (twice the clusters).

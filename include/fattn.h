@@ -25,6 +25,13 @@
  * Asynchrony.  fattn_fwd enqueues the work on ``stream`` and returns; results
  * are visible after the stream is synchronised.
  *
+ * Threads.  Every entry point may be called from any host thread; calls on
+ * different streams are independent (the no-alloc cache entry excepted, see
+ * there).  A call works on the thread's current device; on a thread with no
+ * current context it binds that device's primary context to the thread.
+ * The device status block is shared by all calls on a device, so a status
+ * read by fattn_last_error may come from another thread's call.
+ *
  * Errors.  Every entry point returns FATTN_OK (0) or a negative status; none
  * aborts, throws or falls back to another implementation.  Argument errors are
  * detected on the host before anything is enqueued.  An error inside a
