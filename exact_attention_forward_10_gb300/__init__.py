@@ -9,8 +9,10 @@ calling into a missing library raises.
     o, lse = forward_kvcache(q_new, k_cache, v_cache, cache_lens)  # decoding
 
 ``q, k, v``: contiguous ``[B, H, S, D]`` fp16 or bf16 CUDA tensors, D in
-{64, 128}.  Returns ``o`` (same shape and dtype) and ``lse`` (``[B, H, S]``
-fp32, natural log of the row's softmax normaliser over scaled scores).
+{64, 128, 256}.  Returns ``o`` (same shape and dtype) and ``lse``
+(``[B, H, S]`` fp32, natural log of the row's softmax normaliser over scaled
+scores).  The library works on the calling thread's current device; the
+torch wrappers make q's device current for the call.
 """
 from __future__ import annotations
 
@@ -201,9 +203,10 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None,
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    rc = fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
-                   lse.data_ptr(), B, H, S, D, causal, scale, _dtype_code(q),
-                   stream.cuda_stream)
+    with torch.cuda.device(q.device):
+        rc = fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                       lse.data_ptr(), B, H, S, D, causal, scale, _dtype_code(q),
+                       stream.cuda_stream)
     if rc != FATTN_OK:
         raise FattnError(rc)
     return out, lse
@@ -250,11 +253,12 @@ def forward_kvcache(q, k_cache, v_cache, cache_lens=None, causal: bool = False,
         workspace = torch.empty(max(16, need), dtype=torch.uint8, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
-    rc = fattn_fwd_kvcache(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                           lens_ptr, out.data_ptr(), lse.data_ptr(), B, H, Sq,
-                           Sk, D, causal, scale, _dtype_code(q),
-                           workspace.data_ptr(), workspace.numel(),
-                           stream.cuda_stream)
+    with torch.cuda.device(q.device):
+        rc = fattn_fwd_kvcache(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                               lens_ptr, out.data_ptr(), lse.data_ptr(), B, H, Sq,
+                               Sk, D, causal, scale, _dtype_code(q),
+                               workspace.data_ptr(), workspace.numel(),
+                               stream.cuda_stream)
     if rc != FATTN_OK:
         raise FattnError(rc, "fattn_fwd_kvcache")
     return out, lse
@@ -285,9 +289,10 @@ def forward_fp8(q8, k8, v8, q_scale: float, k_scale: float, v_scale: float,
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q8.device)
     if stream is None:
         stream = torch.cuda.current_stream(q8.device)
-    rc = fattn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(),
-                       lse.data_ptr(), B, H, S, D, causal, scale, q_scale, k_scale,
-                       v_scale, code, stream.cuda_stream)
+    with torch.cuda.device(q8.device):
+        rc = fattn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), B, H, S, D, causal, scale, q_scale, k_scale,
+                           v_scale, code, stream.cuda_stream)
     if rc != FATTN_OK:
         raise FattnError(rc, "fattn_fwd_fp8")
     return out, lse
