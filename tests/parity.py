@@ -1,8 +1,8 @@
 """Shared parity helpers for the GPU tests: run the CUDA path through the C
 ABI, run the oracle, compare with the stated tolerances.
 
-Tolerances (stated in the task's target for this path): fp16 max|O - O_ref|
-<= 2e-3, bf16 <= 1.5e-2, |LSE - LSE_ref| <= 1e-3.  Reading adopted for the
+Tolerances (the library's accuracy targets): fp16 max|O - O_ref| <= 2e-3,
+bf16 <= 1.5e-2, |LSE - LSE_ref| <= 1e-3.  Reading adopted for the
 bf16 floor: casting O to bf16 alone can miss by half a unit in the last place,
 which exceeds 1.5e-2 once |O_ref| >= 4 (spacing 2^-5 there), so an element
 with |O_ref| >= 4 also passes when its error is within 1.5e-2 plus half an
