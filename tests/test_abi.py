@@ -1,6 +1,7 @@
 """The C-ABI library: it loads without a GPU, exports every entry point that
 include/fattn.h declares, and rejects bad arguments on the host before any
-CUDA call (so these run on a CPU-only machine)."""
+CUDA call (so these run on a CPU-only machine).  Without the library nothing
+computes: the binding raises, and host tensors are refused."""
 import ctypes
 import os
 import re
@@ -158,3 +159,29 @@ def test_fp8_host_side_rejections(lib, args, want):
 def test_wait_check_rejects_out_of_range_limits(lib):
     for us in (0, -5, 1000001):
         assert fattn.fattn_check_wait_timeout(us, 0) == fattn.FATTN_ERR_INVALID_ARG
+
+
+def test_missing_library_raises(monkeypatch, tmp_path):
+    """No library, no computation: every entry point goes through ``lib()``,
+    which raises instead of falling back to anything else."""
+    monkeypatch.setattr(fattn, "LIB_PATH", str(tmp_path / "libfattn.so"))
+    monkeypatch.setattr(fattn, "_lib", None)
+    with pytest.raises(ImportError):
+        fattn.lib()
+    with pytest.raises(ImportError):
+        fattn.fattn_fwd(16, 16, 16, 16, 16, 1, 1, 128, 64, 0, 0.125, 0, 0)
+    with pytest.raises(ImportError):
+        fattn.fattn_version()
+
+
+def test_host_tensors_are_rejected():
+    """The torch wrappers take CUDA tensors only; there is no host path."""
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        fattn.forward(q, q, q)
+    with pytest.raises(ValueError):
+        fattn.forward_kvcache(q[:, :, :1], q, q)
+    q8 = torch.zeros(1, 1, 128, 128, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        fattn.forward_fp8(q8, q8, q8, 1.0, 1.0, 1.0)
