@@ -107,6 +107,29 @@ def test_reference_moves_inside_a_tile(jstar, dtype):
         check_full(x, causal, f"jump at key {jstar} {dtype} causal={causal}")
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_zero_queries(D, dtype, causal):
+    """Q = 0: every allowed score is 0, every weight 1, so O is the mean of
+    the allowed V rows (a prefix mean when causal) and LSE the log of their
+    count."""
+    x = attn_inputs.make_qkv(1, 2, 300, D, dtype, seed=6800 + D)
+    x.q[:] = 0.0
+    check_full(x, causal, f"Q=0 D{D} {dtype} causal={causal}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_constant_value_rows(D, dtype, causal):
+    """Every V row the same vector: any convex combination of them is that
+    vector, whatever the scores."""
+    x = attn_inputs.make_qkv(1, 2, 300, D, dtype, seed=6900 + D)
+    x.v[:] = x.v[0, 0, 0]
+    check_full(x, causal, f"constant V D{D} {dtype} causal={causal}")
+
+
 def test_many_heads_short_sequences():
     x = attn_inputs.make_qkv(8, 64, 256, 64, "fp16", seed=11)
     for causal in (False, True):
