@@ -2,7 +2,6 @@
 include/fattn.h declares, and rejects bad arguments on the host before any
 CUDA call (so these run on a CPU-only machine).  Without the library nothing
 computes: the binding raises, and host tensors are refused."""
-import ctypes
 import os
 import re
 

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import attn_inputs
-from parity import check_kvcache, compare_kvcache, run_cuda_kvcache
+from parity import check_kvcache, run_cuda_kvcache
 
 pytestmark = pytest.mark.gpu
 

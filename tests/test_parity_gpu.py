@@ -6,7 +6,6 @@ times) on sampled rows.  Output buffers are NaN-poisoned first, so an
 unwritten element fails.
 """
 import json
-import math
 import os
 
 import numpy as np
