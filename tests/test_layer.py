@@ -119,6 +119,8 @@ def test_attention_call_allocates_no_score_matrix(cuda):
 
 @pytest.mark.gpu
 def test_layer_is_faster_than_materialising_layer(cuda):
+    """At least 3x faster, the gate the notebook sets for its kernel layer
+    against the materialising one (measured: 0.28 against 2.67 ms)."""
     torch.manual_seed(0)
     layer = L.ExactAttention(4096, 32, device=cuda, dtype=torch.float16)
     x = torch.randn(1, 2048, 4096, device=cuda, dtype=torch.float16)
@@ -139,4 +141,4 @@ def test_layer_is_faster_than_materialising_layer(cuda):
     t_fused = timed(lambda: layer(x))
     t_naive = timed(lambda: _materialising_attention(layer, x))
     print(f"layer B1 T2048 d4096 H32: fused {t_fused:.3f} ms, materialising {t_naive:.3f} ms")
-    assert t_fused * 1.5 < t_naive
+    assert t_fused * 3.0 < t_naive
