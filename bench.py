@@ -502,9 +502,27 @@ def cpu_baseline(x, w) -> dict:
                       f"({dt:.1f} s); metric FLOPs of those rows / wall time"}
 
 
+SWEEP_CSV_FIELDS = ("seqlen", "headdim", "dtype", "causal", "ms_median", "tflops",
+                    "frac_of_measured_peak")
+
+
+def write_sweep_csv(path: str, records) -> None:
+    """The sweep as CSV, one row per (S, D, dtype, mask) point, in the
+    columns of the sweep's JSON lines (S as seqlen, D as headdim)."""
+    import csv
+    with open(path, "w", newline="") as f:
+        out = csv.writer(f)
+        out.writerow(SWEEP_CSV_FIELDS)
+        for r in records:
+            out.writerow([r["S"], r["D"], r["dtype"], int(bool(r["causal"])),
+                          f"{r['ms_median']:.6f}", f"{r['tflops']:.3f}",
+                          f"{r['frac_of_measured_peak']:.4f}"])
+
+
 def run_sweep(args):
     """Attention TFLOPS over the sweep shapes (B2 H16; S 512 .. 16384 and
-    4097; D 64, 128; fp16, bf16; both masks): one JSON line per point.
+    4097; D 64, 128; fp16, bf16; both masks): one JSON line per point, and
+    with ``--csv PATH`` the same points as CSV.
     Timing inputs come from torch's generator on the device (the same i.i.d.
     N(0,1) distribution; parity over these shapes is the tests' job)."""
     import torch
@@ -520,6 +538,7 @@ def run_sweep(args):
         shapes += [attn_inputs.Workload(f"B2_H16_S{S}_D256_{dt}", 2, 16, S, 256, dt,
                                         (False, True), 100)
                    for S in attn_inputs.SWEEP_S for dt in attn_inputs.DTYPES]
+    records = []
     for w in shapes:
         tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
         code = fattn.FATTN_BF16 if w.dtype == "bf16" else fattn.FATTN_FP16
@@ -555,9 +574,13 @@ def run_sweep(args):
             if rc != 0:
                 raise RuntimeError(f"kernel status {rc} at {where}")
             tf = metric_flops(w.B, w.H, w.S, w.D, causal) / (ms * 1e-3) / 1e12
-            print(json.dumps({"S": w.S, "D": w.D, "dtype": w.dtype, "causal": causal,
-                              "ms_median": ms, "tflops": tf,
-                              "frac_of_measured_peak": tf / peaks["burst"]}), flush=True)
+            rec = {"S": w.S, "D": w.D, "dtype": w.dtype, "causal": causal,
+                   "ms_median": ms, "tflops": tf,
+                   "frac_of_measured_peak": tf / peaks["burst"]}
+            records.append(rec)
+            print(json.dumps(rec), flush=True)
+    if args.csv:
+        write_sweep_csv(args.csv, records)
     return 0
 
 
@@ -984,6 +1007,8 @@ def main():
                     help="S,D,dtype (B2 H16) to use as the step workload instead of "
                          "B2 H16 S8192 D128 bf16, e.g. 8192,64,bf16 or 8192,256,bf16 "
                          "(sweep shapes keep their seeds; others use seed 100)")
+    ap.add_argument("--csv", default=None, metavar="PATH",
+                    help="with --sweep: also write the points to PATH as CSV")
     ap.add_argument("--dims", default="64,128",
                     help="head dims of --sweep (64,128 are the sweep's; 256 adds the "
                          "CTA-pair kernel)")

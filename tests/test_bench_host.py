@@ -1,11 +1,12 @@
 """Host-side logic of ``bench.py``, on the CPU: the metric's FLOP count and
 the cache path's algorithmic bytes, the rule that a stored ncu traffic
 figure is used only for the kernel sources it was measured on, the peaks
-file, and the JSON line of the reference arm (the fp64 oracle on the host
-cores), which prints on rank 0 only."""
+file, the JSON line of the reference arm (the fp64 oracle on the host
+cores), which prints on rank 0 only, and the sweep's CSV."""
 from __future__ import annotations
 
 import argparse
+import csv
 import io
 import json
 import os
@@ -146,3 +147,18 @@ def test_reference_arm_prints_on_rank_zero_only(monkeypatch):
     monkeypatch.setattr(bench, "calibrate_rows", lambda x, w, target_s: 32)
     rc, out = _run(bench.run_reference, _args(1, 0))
     assert rc == 0 and out == ""
+
+
+def test_sweep_csv(tmp_path):
+    recs = [{"S": 512, "D": 64, "dtype": "fp16", "causal": False, "ms_median": 0.0184,
+             "tflops": 116.9, "frac_of_measured_peak": 0.0613},
+            {"S": 4097, "D": 128, "dtype": "bf16", "causal": True, "ms_median": 0.4,
+             "tflops": 1010.0, "frac_of_measured_peak": 0.53}]
+    path = tmp_path / "sweep.csv"
+    bench.write_sweep_csv(str(path), recs)
+    with open(path, newline="") as f:
+        rows = list(csv.reader(f))
+    assert tuple(rows[0]) == bench.SWEEP_CSV_FIELDS
+    assert rows[1][:4] == ["512", "64", "fp16", "0"]
+    assert rows[2][:4] == ["4097", "128", "bf16", "1"]
+    assert float(rows[2][5]) == 1010.0 and float(rows[1][4]) == pytest.approx(0.0184)
