@@ -1,0 +1,88 @@
+"""The oracle and the CUDA path share no code (static checks on the CPU).
+
+* Nothing in the package (Python binding, layer, build script, CUDA sources
+  and headers) or in include/ imports, includes or loads anything of the
+  oracle's.
+* The oracle imports nothing of the package and includes no CUDA source.
+* ``attn_inputs``, the one module both sides use, imports neither.
+* ``bench.py`` loads the oracle only inside its CPU-baseline and
+  reference-arm functions, never at module level.
+"""
+from __future__ import annotations
+
+import ast
+import os
+import re
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+PKG = os.path.join(ROOT, "exact_attention_forward_10_gb300")
+
+# functions of bench.py allowed to import the oracle
+BENCH_ORACLE_USERS = {"cpu_oracle_run", "kv_oracle_run"}
+
+
+def _files(top, exts):
+    for d, dirs, fs in os.walk(top):
+        dirs[:] = [x for x in dirs if not x.startswith(("_build", "__pycache__"))]
+        for f in fs:
+            if f.endswith(exts):
+                yield os.path.join(d, f)
+
+
+def _python_imports(path):
+    tree = ast.parse(open(path).read())
+    out = []
+    for node in ast.walk(tree):
+        if isinstance(node, ast.Import):
+            out += [a.name.split(".")[0] for a in node.names]
+        elif isinstance(node, ast.ImportFrom) and node.module and node.level == 0:
+            out.append(node.module.split(".")[0])
+    return out
+
+
+def test_product_never_touches_the_oracle():
+    for path in _files(PKG, (".py",)):
+        assert "oracle" not in _python_imports(path), path
+        assert "liboracle" not in open(path).read(), path
+    for path in list(_files(os.path.join(PKG, "csrc"), (".cu", ".cuh", ".h"))) + \
+            list(_files(os.path.join(ROOT, "include"), (".h",))):
+        text = open(path).read()
+        for inc in re.findall(r'#include\s+[<"]([^>"]+)[>"]', text):
+            assert "oracle" not in inc, (path, inc)
+        assert "attn_oracle" not in text and "liboracle" not in text, path
+
+
+def test_oracle_never_touches_the_product():
+    for path in _files(os.path.join(ROOT, "oracle"), (".py",)):
+        imps = _python_imports(path)
+        assert "exact_attention_forward_10_gb300" not in imps, path
+        assert "torch" not in imps, path
+    for path in _files(os.path.join(ROOT, "oracle"), (".c", ".h")):
+        text = open(path).read()
+        for inc in re.findall(r'#include\s+[<"]([^>"]+)[>"]', text):
+            assert not inc.startswith(("fattn", "ptx", "cuda")), (path, inc)
+
+
+def test_shared_input_module_imports_neither_side():
+    for path in _files(os.path.join(ROOT, "attn_inputs"), (".py",)):
+        imps = _python_imports(path)
+        assert "oracle" not in imps and "exact_attention_forward_10_gb300" not in imps, path
+
+
+def test_bench_loads_the_oracle_only_in_its_baseline_functions():
+    tree = ast.parse(open(os.path.join(ROOT, "bench.py")).read())
+    users = set()
+
+    def visit(node, func):
+        for child in ast.iter_child_nodes(node):
+            f = child.name if isinstance(child, (ast.FunctionDef, ast.AsyncFunctionDef)) else func
+            if isinstance(child, ast.Import) and any(a.name.split(".")[0] == "oracle"
+                                                     for a in child.names):
+                users.add(func)
+            if isinstance(child, ast.ImportFrom) and (child.module or "").split(".")[0] == "oracle":
+                users.add(func)
+            visit(child, f)
+
+    visit(tree, None)
+    assert None not in users, "bench.py imports the oracle at module level"
+    assert users <= BENCH_ORACLE_USERS, users
