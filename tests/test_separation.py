@@ -7,6 +7,9 @@
 * ``attn_inputs``, the one module both sides use, imports neither.
 * ``bench.py`` loads the oracle only inside its CPU-baseline and
   reference-arm functions, never at module level.
+* The Python side of the path (binding and layer) holds no attention
+  arithmetic and no library or compiler route to one, so nothing can fall
+  back from the kernels silently.
 """
 from __future__ import annotations
 
@@ -86,3 +89,30 @@ def test_bench_loads_the_oracle_only_in_its_baseline_functions():
     visit(tree, None)
     assert None not in users, "bench.py imports the oracle at module level"
     assert users <= BENCH_ORACLE_USERS, users
+
+
+FORBIDDEN_ON_PATH = ("softmax", "scaled_dot_product_attention", "einsum", "matmul",
+                     "bmm", "logsumexp", "torch.exp", "np.exp", "triton", "torch.compile")
+
+
+def test_python_side_of_the_path_computes_no_attention():
+    """The binding and the layer marshal arguments and run the projections
+    (``nn.Linear``); every step of the attention itself runs in the CUDA
+    kernels, so none of these appear there (no silent host or library
+    fallback)."""
+    for path in _files(PKG, (".py",)):
+        if os.path.basename(path) == "build.py":
+            continue
+        tree = ast.parse(open(path).read())
+        # docstrings (and comments, which the parser drops) may name these
+        # things; the code itself may not
+        for node in ast.walk(tree):
+            body = getattr(node, "body", None)
+            if (isinstance(body, list) and body and isinstance(body[0], ast.Expr)
+                    and isinstance(body[0].value, ast.Constant)
+                    and isinstance(body[0].value.value, str)):
+                node.body = body[1:] or [ast.Pass()]
+        code = ast.unparse(tree)
+        for word in FORBIDDEN_ON_PATH:
+            assert word not in code, (path, word)
+        assert " @ " not in code, (path, "matrix product")
