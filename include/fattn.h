@@ -259,7 +259,8 @@ FATTN_API int fattn_kvcache_plan(int B, int H, int Sq, int Sk, int D,
  * [0, Sk], a pipeline wait past its limit) are recorded there as
  * fattn_last_error would report them: word 0 the status, word 1 where, word 2
  * the block or batch index.  With NULL they go to a private static word that
- * is never read.
+ * is never read: fattn_last_error does not see errors of this entry point in
+ * either case, so a caller that needs them passes status_words.
  *
  * Every other argument, layout and return code as fattn_fwd_kvcache.
  */

@@ -11,6 +11,7 @@ ulp of the dtype at O_ref.  The literal maximum error is always reported.
 from __future__ import annotations
 
 import math
+import warnings
 
 import numpy as np
 
@@ -56,14 +57,19 @@ def run_cuda(x: attn_inputs.QKV, causal: bool, scale: float | None = None,
     return o.double().cpu().numpy(), lse.double().cpu().numpy()
 
 
-def sample_rows(B: int, H: int, S: int, seed: int, n_heads: int = 3,
-                stride: int = 16):
-    """Global row indices: in a few heads (first, last, seeded others), every
-    row of the first and last 128-row tiles plus a seeded 1-in-``stride``
-    sample of the rest."""
+def sample_rows(B: int, H: int, S: int, seed: int, n_heads: int | None = None,
+                stride: int = 64):
+    """Global row indices: every row of the first and last 128-row tiles plus
+    a seeded 1-in-``stride`` sample of the rest, in every (batch, head) by
+    default (the persistent schedule gives each head's work units to
+    different CTAs and rounds), or with ``n_heads`` in a few heads only
+    (first, last, seeded others)."""
     rng = np.random.default_rng(seed)
     BH = B * H
-    heads = sorted({0, BH - 1, *rng.integers(0, BH, size=max(0, n_heads - 2)).tolist()})
+    if n_heads is None:
+        heads = list(range(BH))
+    else:
+        heads = sorted({0, BH - 1, *rng.integers(0, BH, size=max(0, n_heads - 2)).tolist()})
     rows = []
     for bh in heads:
         r = set(range(min(S, 128)))
@@ -88,6 +94,11 @@ def compare(o, lse, ro, rl, dtype: str, label: str = ""):
             f"{label}: O mismatch at {idx}: got {o[idx]}, want {ro[idx]} "
             f"(max|dO|={e_o:.3e}, {int((~ok).sum())} elements out of tolerance)")
     assert e_l <= TOL_LSE, f"{label}: max|dLSE|={e_l:.3e} > {TOL_LSE}"
+    n_ulp = int((err > tol).sum())
+    if n_ulp:
+        # within the per-element reading only: say so in the run's summary
+        warnings.warn(f"{label}: {n_ulp} elements exceed the flat bound {tol} and pass "
+                      f"through the half-ulp allowance at |O_ref| >= 4 (max|dO|={e_o:.3e})")
     return e_o, e_l
 
 
@@ -101,7 +112,7 @@ def check_full(x: attn_inputs.QKV, causal: bool, label: str = ""):
 
 
 def check_sampled(x: attn_inputs.QKV, causal: bool, seed: int, label: str = "",
-                  stride: int = 16, n_heads: int = 3):
+                  stride: int = 64, n_heads: int | None = None):
     """Sampled rows against the oracle (full-size workloads)."""
     B, H, S, D = x.q.shape
     scale = 1.0 / math.sqrt(D)

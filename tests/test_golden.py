@@ -2,8 +2,8 @@
 
 ``tiny_fp16_noncausal_oracle.json`` was written by ``make_golden.py`` from the
 fp64 oracle; a change to the oracle's arithmetic shows up here first.
-``pages_values.json`` holds the figures the pages print (with citations); the
-package's host-side helpers must reproduce them.
+``pages_values.json`` holds figures the pages print (with their citation);
+the package's host-side helpers must reproduce them.
 """
 import json
 import os
@@ -26,3 +26,11 @@ def test_tiny_oracle_fixture():
     flat = o.reshape(-1, w.D)
     for r, vals in g["o_rows"].items():
         np.testing.assert_allclose(flat[int(r)], vals, rtol=0, atol=1e-12)
+
+
+def test_pages_score_matrix_figures():
+    from exact_attention_forward_10_gb300 import layer
+    with open(os.path.join(HERE, "pages_values.json")) as f:
+        g = json.load(f)["score_matrix"]
+    assert layer.score_matrix_bytes(1, 1, g["T"], g["dtype_bytes"]) == g["bytes_per_head"]
+    assert layer.score_matrix_bytes(g["B"], g["H"], g["T"], g["dtype_bytes"]) == g["bytes_per_batch"]

@@ -129,3 +129,29 @@ def test_kernel_errors_reach_the_caller_status_words(torch_cuda):
     torch.cuda.synchronize()
     s = status.cpu().tolist()
     assert s[0] == fattn.FATTN_ERR_INVALID_ARG and s[1] >> 8 == 6 and s[2] == 1
+
+
+@pytest.mark.gpu
+def test_repeated_calls_leave_device_memory_unchanged(torch_cuda):
+    """After the first call on the device (which may load the kernels'
+    module), further calls change nothing in the device's free memory."""
+    torch = torch_cuda
+    x = attn_inputs.make_kvcache(4, 8, 2, 1500, 128, "bf16", seed=3103, lens_range=(1, 1500))
+    q, k, v, lens = _device_inputs(torch, x)
+    B, H, Sq, D = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+
+    def call():
+        rc = fattn.fattn_fwd_kvcache_noalloc(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), lens.data_ptr(), o.data_ptr(),
+            lse.data_ptr(), B, H, Sq, k.shape[2], D, 1, 1.0 / math.sqrt(D),
+            fattn.FATTN_BF16, 0, torch.cuda.current_stream().cuda_stream)
+        assert rc == fattn.FATTN_OK, fattn.fattn_error_string(rc)
+        torch.cuda.synchronize()
+
+    call()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        call()
+    assert torch.cuda.mem_get_info()[0] == free0
