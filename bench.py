@@ -55,6 +55,76 @@ def row_flops(S, D, causal) -> float:
     return (2.0 if causal else 4.0) * S * D
 
 
+def algo_bytes(B, H, S, D) -> int:
+    """Algorithmic HBM bytes of one launch: Q, K, V read once, O and the
+    fp32 LSE written once (16-bit tensors)."""
+    return B * H * S * (8 * D + 4)
+
+
+# Accuracy targets of the library: max|O - O_ref| 2e-3 (fp16) / 1.5e-2 (bf16),
+# |LSE - LSE_ref| 1e-3.  An element with |O_ref| >= 4 also passes within the
+# flat bound plus half a unit in the last place of the 16-bit dtype there
+# (the final cast alone can miss by that much); how many elements needed that
+# allowance is reported beside the flat result.
+TOL_O = {"fp16": 2e-3, "bf16": 1.5e-2}
+TOL_LSE = 1e-3
+MANT_BITS = {"fp16": 10, "bf16": 7}
+
+
+def parity_stats(o, lse, ro, rl, dtype: str) -> dict:
+    """Worst errors of GPU rows (o [n, D], lse [n]) against the oracle's."""
+    o, lse, ro, rl = (np.asarray(a, dtype=np.float64) for a in (o, lse, ro, rl))
+    finite = bool(np.isfinite(o).all() and np.isfinite(lse).all())
+    err = np.abs(o - ro)
+    tol = TOL_O[dtype]
+    ax = np.maximum(np.abs(ro), 2.0 ** -14)
+    half_ulp = 0.5 * np.exp2(np.floor(np.log2(ax)) - MANT_BITS[dtype])
+    flat_ok = err <= tol
+    ok = flat_ok | ((np.abs(ro) >= 4.0) & (err <= tol + half_ulp))
+    dl = np.abs(lse - rl)
+    e_o = float(err.max()) if err.size else 0.0
+    e_l = float(dl.max()) if dl.size else 0.0
+    return {"rows": int(o.shape[0]), "max_abs_dO": e_o, "max_abs_dLSE": e_l,
+            "tol_O": tol, "tol_LSE": TOL_LSE, "flat_pass": bool(flat_ok.all()) and finite,
+            "n_pass_by_ulp_allowance": int((ok & ~flat_ok).sum()),
+            "pass": bool(ok.all()) and e_l <= TOL_LSE and finite}
+
+
+def merge_parity(parts) -> dict:
+    """One block over several (mask) comparisons: worst errors, all passes."""
+    parts = list(parts)
+    return {"rows": sum(p["rows"] for p in parts),
+            "max_abs_dO": max(p["max_abs_dO"] for p in parts),
+            "max_abs_dLSE": max(p["max_abs_dLSE"] for p in parts),
+            "tol_O": parts[0]["tol_O"], "tol_LSE": TOL_LSE,
+            "flat_pass": all(p["flat_pass"] for p in parts),
+            "n_pass_by_ulp_allowance": sum(p["n_pass_by_ulp_allowance"] for p in parts),
+            "pass": all(p["pass"] for p in parts)}
+
+
+def head_rows(B: int, H: int, S: int, seed: int, edge: int = 16, inner: int = 8):
+    """Rows of every (batch, head): the first and last ``edge`` rows and
+    ``inner`` seeded others (all rows when S is small)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for bh in range(B * H):
+        if S <= 2 * edge + inner:
+            r = np.arange(S)
+        else:
+            mid = rng.choice(np.arange(edge, S - edge), size=inner, replace=False)
+            r = np.concatenate([np.arange(edge), np.sort(mid), np.arange(S - edge, S)])
+        out.append(bh * S + r)
+    return np.concatenate(out).astype(np.int64)
+
+
+def gather_rows(torch, o, lse, rows):
+    """Rows (global indices into [B*H*S]) of device outputs, as fp64 numpy."""
+    idx = torch.as_tensor(rows, dtype=torch.long, device=o.device)
+    D = o.shape[-1]
+    return (o.reshape(-1, D).index_select(0, idx).double().cpu().numpy(),
+            lse.reshape(-1).index_select(0, idx).double().cpu().numpy())
+
+
 def workload_config(w, extra=None) -> dict:
     c = {"workload": f"B{w.B} H{w.H} S{w.S} D{w.D} {w.dtype}, non-causal + "
                      f"causal, Q/K/V iid N(0,1) seed {w.seed}, scale 1/sqrt(D)",
@@ -76,6 +146,159 @@ def load_peaks() -> dict:
                 "sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
                 "source": "measured"}
     return {"burst": 1900.0, "sustained": 1700.0, "source": "fallback"}
+
+
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read through NVML (the
+    driver's libnvidia-ml, read-only queries) every ``period_s`` while the
+    timed region runs, so a region of a few tens of milliseconds still
+    gives tens of samples.  ``ok`` is False when NVML cannot be used."""
+
+    # clock-event reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, pci_bus_id: str | None, index: int, period_s: float = 0.0005):
+        import ctypes
+        self.period = period_s
+        self.samples = []
+        self.thread = None
+        self.stop_flag = threading.Event()
+        self.ok = False
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            rc = -1
+            if pci_bus_id:
+                rc = self.nvml.nvmlDeviceGetHandleByPciBusId_v2(
+                    pci_bus_id.encode(), ctypes.byref(self.handle))
+            if rc != 0:
+                rc = self.nvml.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.handle))
+            if rc != 0:
+                return
+            fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None)
+            self.reasons_fn = fn or self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            self.max_mhz = (mx.value if self.nvml.nvmlDeviceGetMaxClockInfo(
+                self.handle, 1, ctypes.byref(mx)) == 0 else None)
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def _read(self):
+        import ctypes
+        mhz, reasons, mw = ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
+        while not self.stop_flag.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
+                r = reasons.value if self.reasons_fn(self.handle, ctypes.byref(reasons)) == 0 else 0
+                w = mw.value / 1000.0 if self.nvml.nvmlDeviceGetPowerUsage(
+                    self.handle, ctypes.byref(mw)) == 0 else None
+                self.samples.append((mhz.value, r, w))
+            time.sleep(self.period)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def stop(self) -> dict:
+        self.stop_flag.set()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm = [s[0] for s in self.samples]
+        reasons = set()
+        for _, r, _ in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    reasons.add(name)
+        power = [s[2] for s in self.samples if s[2] is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_min_mhz": min(sm) if sm else None,
+                "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "source": f"NVML every {self.period * 1e3:.1f} ms",
+                "reasons": sorted(reasons)}
+
+
+def clock_sampler(dev):
+    """The NVML sampler when NVML answers, else nvidia-smi."""
+    s = NvmlClockSampler(gpu_pci_bus_id(dev), dev.index)
+    return s if s.ok else ClockSampler(dev.index)
+
+
+def gpu_pci_bus_id(dev) -> str | None:
+    """``domain:bus:device.0`` of the GPU, from torch's device properties."""
+    import torch
+    p = torch.cuda.get_device_properties(dev)
+    if not all(hasattr(p, a) for a in ("pci_domain_id", "pci_bus_id", "pci_device_id")):
+        return None
+    return f"{p.pci_domain_id:04x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+
+
+def gpu_local_cpus(dev):
+    """The host CPUs on the GPU's side of the machine (the PCI device's
+    ``local_cpulist`` in sysfs) and its NUMA node; (None, None) when the
+    system does not say."""
+    bus = gpu_pci_bus_id(dev)
+    if bus is None:
+        return None, None
+    base = f"/sys/bus/pci/devices/{bus}"
+    cpus, node = None, None
+    try:
+        with open(f"{base}/local_cpulist") as f:
+            cpus = set()
+            for part in f.read().strip().split(","):
+                if "-" in part:
+                    a, b = part.split("-")
+                    cpus.update(range(int(a), int(b) + 1))
+                elif part:
+                    cpus.add(int(part))
+        with open(f"{base}/numa_node") as f:
+            node = int(f.read().strip())
+    except (OSError, ValueError):
+        pass
+    return cpus, node
+
+
+def pinned_near_gpu(dev, make):
+    """Run ``make()`` (which allocates pinned host buffers) with this thread
+    on the GPU's local CPUs, so first-touch places the pages on that side of
+    the machine; the previous affinity is restored afterwards.  Returns
+    (make's result, a note saying what was done)."""
+    cpus, node = gpu_local_cpus(dev)
+    old = os.sched_getaffinity(0)
+    use = (cpus & old) if cpus else None
+    if not use or use == old:
+        note = (f"pinned buffers allocated from the process's CPUs "
+                f"({len(old)}; GPU-local CPU list {'equal' if use else 'not available'})")
+        return make(), note
+    os.sched_setaffinity(0, use)
+    try:
+        out = make()
+    finally:
+        os.sched_setaffinity(0, old)
+    return out, (f"pinned buffers allocated with the thread on the GPU's {len(use)} local CPUs "
+                 f"(NUMA node {node}) of {len(old)}")
+
+
+def copy_gbs(torch, dev, stream, src, dst, reps: int = 5) -> float:
+    """GB/s of copying ``src`` into ``dst`` (one list of tensors each way),
+    each copy alone on ``stream``, best of ``reps``."""
+    nbytes = sum(t.numel() * t.element_size() for t in src)
+    best = None
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            for d, s_ in zip(dst, src):
+                d.copy_(s_, non_blocking=True)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    return nbytes / (best * 1e-3) / 1e9
 
 
 class ClockSampler:
@@ -207,18 +430,23 @@ def oracle_sample_rows(w, n_rows: int, seed: int) -> np.ndarray:
     return np.sort(rng.choice(w.B * w.H * w.S, size=n_rows, replace=False))
 
 
-def cpu_oracle_run(x, w, rows_per_mask: int, seed: int):
+def cpu_oracle_run(x, w, rows_per_mask: int, seed: int, keep: bool = False):
     """Oracle on ``rows_per_mask`` sampled rows per mask; returns (seconds,
-    metric FLOPs of those rows, threads)."""
+    metric FLOPs of those rows, threads, and with ``keep`` a dict mask ->
+    (rows, O rows, LSE rows))."""
     import oracle
     threads = oracle.default_threads()
     flops = 0.0
+    outs = {}
     t0 = time.perf_counter()
     for m, causal in enumerate(MASKS):
         rows = oracle_sample_rows(w, rows_per_mask, seed + m)
-        oracle.attn_fwd(x.q, x.k, x.v, causal, w.scale, rows=rows, threads=threads)
+        ro, rl = oracle.attn_fwd(x.q, x.k, x.v, causal, w.scale, rows=rows, threads=threads)
+        if keep:
+            outs[causal] = (rows, ro, rl)
         flops += rows_per_mask * row_flops(w.S, w.D, causal)
-    return time.perf_counter() - t0, flops, threads
+    dt = time.perf_counter() - t0
+    return (dt, flops, threads, outs) if keep else (dt, flops, threads)
 
 
 def calibrate_rows(x, w, target_s: float) -> int:
@@ -285,7 +513,8 @@ def run_fattn(args):
     b0, b1 = shard.batch_range(global_b, world, rank)
     x = (w.inputs() if world == 1 else
          attn_inputs.make_qkv_shard(global_b, b0, b1, w.H, w.S, w.D, w.dtype, w.seed))
-    host = [torch.from_numpy(a).to(tdt).pin_memory() for a in (x.q, x.k, x.v)]
+    host, placement = pinned_near_gpu(
+        dev, lambda: [torch.from_numpy(a).to(tdt).pin_memory() for a in (x.q, x.k, x.v)])
     q, k, v = (h.to(dev) for h in host)
     B, H, S, D = b1 - b0, w.H, w.S, w.D
     outs = {c: (torch.empty_like(q), torch.empty((B, H, S), dtype=torch.float32, device=dev))
@@ -324,9 +553,9 @@ def run_fattn(args):
             for c in MASKS:
                 launch(c, q, k, v)
     barrier()
-    sampler = ClockSampler(dev.index)
+    sampler = clock_sampler(dev)
     sampler.start()
-    time.sleep(0.25)
+    time.sleep(0.05)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -355,8 +584,10 @@ def run_fattn(args):
     # copy overlap step k's kernels (an H2D and a D2H stream beside the compute
     # stream, two device buffers).  The same steps one after another on one
     # stream are reported too (e2e "serial").
-    h_outs = {c: (torch.empty((B, H, S, D), dtype=tdt).pin_memory(),
-                  torch.empty((B, H, S), dtype=torch.float32).pin_memory()) for c in MASKS}
+    h_outs, _ = pinned_near_gpu(
+        dev, lambda: {c: (torch.empty((B, H, S, D), dtype=tdt).pin_memory(),
+                          torch.empty((B, H, S), dtype=torch.float32).pin_memory())
+                      for c in MASKS})
     e2e_steps = max(3, min(args.steps, 20))
 
     def e2e_step():
@@ -390,6 +621,15 @@ def run_fattn(args):
     h2d = sum(h.numel() * h.element_size() for h in host)
     d2h = sum(o.numel() * o.element_size() + l.numel() * l.element_size()
               for o, l in h_outs.values())
+    # each direction's copy alone, so the record shows whether a step is
+    # bound by the host link rather than by the kernels
+    h2d_gbs = copy_gbs(torch, dev, stream, host, [q, k, v])
+    d2h_gbs = copy_gbs(torch, dev, stream,
+                       [t for c in MASKS for t in outs[c]], [t for c in MASKS for t in h_outs[c]])
+    per_config, keep = [], []
+    if rank == 0:
+        per_config, keep = run_per_config(torch, fattn, dev, stream, load_peaks(),
+                                          main_x=x if world == 1 else None, main_w=w)
 
     # ---- max over ranks
     step_ms, e2e_ms, e2e_serial_ms = shard.max_over_ranks(
@@ -404,7 +644,8 @@ def run_fattn(args):
         ms = statistics.median(per_launch[c])
         tf = metric_flops(B, H, S, D, c) / (ms * 1e-3) / 1e12
         per_mask["causal" if c else "noncausal"] = {
-            "ms_median": ms, "tflops": tf, "frac_of_measured_burst": tf / peaks["burst"]}
+            "ms_median": ms, "tflops": tf, "frac_of_measured_burst": tf / peaks["burst"],
+            "hbm_gbs": algo_bytes(B, H, S, D) / (ms * 1e-3) / 1e9}
     # dominant kernel: the non-causal launch (2/3 of the step's FLOPs)
     dom_ms = statistics.mean(per_launch[False])
     achieved = metric_flops(B, H, S, D, False) / (dom_ms * 1e-3) / 1e12
@@ -412,11 +653,17 @@ def run_fattn(args):
                            "fattn_pair" if D == 256 else "fattn_fwd")
     plan = fattn.fattn_plan(B, H, S, D, False)
 
+    hbm = load_hbm_peak()
+    step_bytes = world * len(MASKS) * algo_bytes(B, H, S, D)
     result = None
     if rank == 0:
-        cpu = None
+        cpu, parity = None, None
         if world == 1 and not args.no_cpu_baseline:
-            cpu = cpu_baseline(x, w)
+            # the oracle leg: its timed sample, then its results on the same
+            # rows compared with the GPU's, and each configuration's rows
+            cpu, oracle_outs = cpu_baseline(x, w, keep=True)
+            parity = oracle_parity(torch, outs, oracle_outs, w.dtype)
+            per_config_parity(per_config, keep)
         result = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -429,6 +676,15 @@ def run_fattn(args):
                                           "grid": plan["grid"], "block": plan["block"],
                                           "units_per_launch": plan["units"]}),
             "per_mask": per_mask,
+            "hbm_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
+            "hbm": {"algorithmic_bytes_per_step": step_bytes,
+                    "frac_of_measured_copy": step_bytes / (step_ms * 1e-3) / 1e9 / hbm["gbs"],
+                    "peak_gbs": hbm["gbs"], "peak_kind": f"HBM copy, {hbm['source']}",
+                    "note": "Q, K, V read once and O, LSE written once per launch over the "
+                            "step time: far below the copy bandwidth, so the step is bound "
+                            "by the tensor pipe, not by HBM"},
+            "parity": parity,
+            "per_config": per_config,
             "roofline": {"bound": "tensor", "achieved": achieved,
                          "peak": peaks["burst"], "unit": "TFLOP/s",
                          "frac": achieved / peaks["burst"],
@@ -441,6 +697,9 @@ def run_fattn(args):
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "schedule": E2E_SCHEDULE,
+                    "h2d_gbs_alone": h2d_gbs, "d2h_gbs_alone": d2h_gbs,
+                    "copy_floor_ms": max(h2d / h2d_gbs, d2h / d2h_gbs) / 1e6,
+                    "host_placement": placement,
                     "serial": {"value": world * flops_step / (e2e_serial_ms * 1e-3) / 1e12,
                                "ms_per_step": e2e_serial_ms}},
             "gpu_launches": args.steps * len(MASKS),
@@ -493,17 +752,128 @@ def load_traffic(key: str = "fattn_fwd_noncausal_bf16_d128", kernel: str = "fatt
     return d.get("bytes_per_launch")
 
 
-def cpu_baseline(x, w) -> dict:
+def cpu_baseline(x, w, keep: bool = False):
+    """The oracle timed on a bounded row sample of the workload (about 15 s
+    of host work); with ``keep`` also its results for those rows (mask ->
+    (rows, O rows, LSE rows)), for the comparison with the GPU's."""
     rows = calibrate_rows(x, w, target_s=15.0)
-    dt, fl, threads = cpu_oracle_run(x, w, rows, 4242)
-    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads,
+    dt, fl, threads, outs = cpu_oracle_run(x, w, rows, 4242, keep=True)
+    line = {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads,
             "kind": "oracle",
             "sample": f"{rows} sampled query rows per mask of {w.name} "
                       f"({dt:.1f} s); metric FLOPs of those rows / wall time"}
+    return (line, outs) if keep else line
+
+
+def oracle_parity(torch, outs_dev, oracle_outs, dtype: str) -> dict:
+    """The GPU's rows (device outputs per mask) against the oracle's rows:
+    one parity block over both masks, and each mask's."""
+    per = {}
+    for causal, (rows, ro, rl) in oracle_outs.items():
+        go, gl = gather_rows(torch, *outs_dev[causal], rows)
+        per["causal" if causal else "noncausal"] = parity_stats(go, gl, ro, rl, dtype)
+    out = merge_parity(per.values())
+    out["per_mask"] = per
+    out["rows_from"] = "the cpu_baseline sample (seeded rows over every batch and head)"
+    return out
+
+
+# The configurations reported one by one beside the step: the small and
+# LLM-layer shapes, the Q,K x4 stress set of the step's shape, and head dim
+# 64 at the step's sequence length (from the sweep, both 16-bit types).
+PER_CONFIG = (("1", "tiny"), ("2", "s2048_d64"), ("3", "s2048_d128"),
+              ("4 Q,K x4", "s8192_d128_x4"),
+              ("5 S8192 D64 fp16", "sweep_S8192_D64_fp16"),
+              ("5 S8192 D64 bf16", "sweep_S8192_D64_bf16"))
+
+
+def per_config_workloads():
+    sweep = {w.name: w for w in attn_inputs.sweep_workloads()}
+    return [(label, attn_inputs.WORKLOADS.get(key) or sweep[key]) for label, key in PER_CONFIG]
+
+
+def time_launches(torch, dev, stream, launch, warmup: int = 10, reps: int = 20) -> float:
+    """Median milliseconds of ``launch()`` over ``reps`` calls, each timed with
+    CUDA events on ``stream``, after ``warmup`` calls."""
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            launch()
+    torch.cuda.synchronize(dev)
+    ev = []
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            launch()
+            b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize(dev)
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+def run_per_config(torch, fattn, dev, stream, peaks, main_x=None, main_w=None):
+    """Times each configuration of PER_CONFIG (every mask it runs) on its
+    seeded input set; returns the records and, per record, what the oracle
+    comparison needs (the host inputs, the mask and the GPU's rows of every
+    batch and head)."""
+    recs, keep = [], []
+    for label, w in per_config_workloads():
+        if (w.qk_mult != 1.0 and main_w is not None and main_x is not None
+                and (w.B, w.H, w.S, w.D, w.dtype, w.seed) ==
+                (main_w.B, main_w.H, main_w.S, main_w.D, main_w.dtype, main_w.seed)):
+            m = np.float32(w.qk_mult)  # a power of two: exact in 16 bits
+            x = attn_inputs.QKV(q=main_x.q * m, k=main_x.k * m, v=main_x.v,
+                                dtype=w.dtype, seed=w.seed, qk_mult=w.qk_mult)
+        else:
+            x = w.inputs()
+        tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+        code = fattn.FATTN_BF16 if w.dtype == "bf16" else fattn.FATTN_FP16
+        q, k, v = (torch.from_numpy(a).to(dev).to(tdt) for a in (x.q, x.k, x.v))
+        o = torch.empty_like(q)
+        lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+        rows = (np.arange(w.B * w.H * w.S, dtype=np.int64) if w.B * w.H * w.S <= 4096
+                else head_rows(w.B, w.H, w.S, seed=w.seed + 7000))
+        for causal in w.causal:
+            def launch():
+                rc = fattn.fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr(), w.B, w.H, w.S, w.D, causal, w.scale,
+                                     code, stream.cuda_stream)
+                if rc != 0:
+                    raise fattn.FattnError(rc)
+            ms = time_launches(torch, dev, stream, launch)
+            rc, where = fattn.fattn_last_error(stream.cuda_stream)
+            if rc != 0:
+                raise RuntimeError(f"kernel status {rc} at {where}")
+            tf = metric_flops(w.B, w.H, w.S, w.D, causal) / (ms * 1e-3) / 1e12
+            recs.append({"config": label, "workload": w.name, "B": w.B, "H": w.H, "S": w.S,
+                         "D": w.D, "dtype": w.dtype, "causal": causal, "seed": w.seed,
+                         "qk_mult": w.qk_mult, "ms_median": ms, "tflops": tf,
+                         "frac_of_measured_burst": tf / peaks["burst"],
+                         "hbm_gbs": algo_bytes(w.B, w.H, w.S, w.D) / (ms * 1e-3) / 1e9,
+                         "parity": None})
+            go, gl = gather_rows(torch, o, lse, rows)
+            keep.append((len(recs) - 1, w, x, causal, rows, go, gl))
+        del q, k, v, o, lse
+    return recs, keep
+
+
+def per_config_parity(recs, keep) -> None:
+    """The oracle on each kept row set; fills each record's parity block."""
+    import oracle
+    threads = oracle.default_threads()
+    for i, w, x, causal, rows, go, gl in keep:
+        t0 = time.perf_counter()
+        ro, rl = oracle.attn_fwd(x.q, x.k, x.v, causal, w.scale, rows=rows, threads=threads)
+        par = parity_stats(go, gl, ro, rl, w.dtype)
+        par["oracle_s"] = time.perf_counter() - t0
+        par["rows_from"] = ("every row" if len(rows) == w.B * w.H * w.S else
+                            "every batch and head: first and last 16 rows and 8 seeded others")
+        recs[i]["parity"] = par
 
 
 SWEEP_CSV_FIELDS = ("seqlen", "headdim", "dtype", "causal", "ms_median", "tflops",
-                    "frac_of_measured_peak")
+                    "frac_of_measured_peak", "hbm_gbs")
 
 
 def write_sweep_csv(path: str, records) -> None:
@@ -516,15 +886,16 @@ def write_sweep_csv(path: str, records) -> None:
         for r in records:
             out.writerow([r["S"], r["D"], r["dtype"], int(bool(r["causal"])),
                           f"{r['ms_median']:.6f}", f"{r['tflops']:.3f}",
-                          f"{r['frac_of_measured_peak']:.4f}"])
+                          f"{r['frac_of_measured_peak']:.4f}", f"{r.get('hbm_gbs', 0.0):.1f}"])
 
 
 def run_sweep(args):
     """Attention TFLOPS over the sweep shapes (B2 H16; S 512 .. 16384 and
     4097; D 64, 128; fp16, bf16; both masks): one JSON line per point, and
     with ``--csv PATH`` the same points as CSV.
-    Timing inputs come from torch's generator on the device (the same i.i.d.
-    N(0,1) distribution; parity over these shapes is the tests' job)."""
+    Each point runs on its seeded input set (seed 4 + index, the sets the
+    parity tests compare with the oracle); generating them on the host takes
+    most of the sweep's wall time."""
     import torch
 
     import exact_attention_forward_10_gb300 as fattn
@@ -542,10 +913,9 @@ def run_sweep(args):
     for w in shapes:
         tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float16
         code = fattn.FATTN_BF16 if w.dtype == "bf16" else fattn.FATTN_FP16
-        g = torch.Generator(device=dev)
-        g.manual_seed(w.seed)
-        q, k, v = (torch.randn(w.B, w.H, w.S, w.D, device=dev, dtype=torch.float32,
-                               generator=g).to(tdt) for _ in range(3))
+        x = w.inputs()
+        q, k, v = (torch.from_numpy(a).to(dev).to(tdt) for a in (x.q, x.k, x.v))
+        del x
         o = torch.empty_like(q)
         lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
         for causal in w.causal:
@@ -574,9 +944,10 @@ def run_sweep(args):
             if rc != 0:
                 raise RuntimeError(f"kernel status {rc} at {where}")
             tf = metric_flops(w.B, w.H, w.S, w.D, causal) / (ms * 1e-3) / 1e12
-            rec = {"S": w.S, "D": w.D, "dtype": w.dtype, "causal": causal,
+            rec = {"S": w.S, "D": w.D, "dtype": w.dtype, "causal": causal, "seed": w.seed,
                    "ms_median": ms, "tflops": tf,
-                   "frac_of_measured_peak": tf / peaks["burst"]}
+                   "frac_of_measured_peak": tf / peaks["burst"],
+                   "hbm_gbs": algo_bytes(w.B, w.H, w.S, w.D) / (ms * 1e-3) / 1e9}
             records.append(rec)
             print(json.dumps(rec), flush=True)
     if args.csv:
@@ -637,9 +1008,9 @@ def run_fp8(args):
     barrier()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps * len(MASKS))]
-    sampler = ClockSampler(dev.index)
+    sampler = clock_sampler(dev)
     sampler.start()
-    time.sleep(0.25)
+    time.sleep(0.05)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
@@ -719,6 +1090,15 @@ def run_fp8(args):
                                                     "scales", "output": "bf16",
                                           "parallelism": f"replicas x{world}"}),
             "per_mask": per_mask,
+            "hbm_gbs": step_bytes / (step_ms * 1e-3) / 1e9,
+            "hbm": {"algorithmic_bytes_per_step": step_bytes,
+                    "frac_of_measured_copy": step_bytes / (step_ms * 1e-3) / 1e9 / hbm["gbs"],
+                    "peak_gbs": hbm["gbs"], "peak_kind": f"HBM copy, {hbm['source']}",
+                    "note": "Q, K, V read once and O, LSE written once per launch over the "
+                            "step time: far below the copy bandwidth, so the step is bound "
+                            "by the tensor pipe, not by HBM"},
+            "parity": parity,
+            "per_config": per_config,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak8,
                          "unit": "TFLOP/s", "frac": achieved / peak8,
                          "peak_kind": (f"fp8 dense = 2 x the {peaks['source']} bf16 burst "
@@ -898,9 +1278,9 @@ def run_kvcache(args, w):
     barrier()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    sampler = ClockSampler(dev.index)
+    sampler = clock_sampler(dev)
     sampler.start()
-    time.sleep(0.25)
+    time.sleep(0.05)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):

@@ -162,3 +162,52 @@ def test_sweep_csv(tmp_path):
     assert rows[1][:4] == ["512", "64", "fp16", "0"]
     assert rows[2][:4] == ["4097", "128", "bf16", "1"]
     assert float(rows[2][5]) == 1010.0 and float(rows[1][4]) == pytest.approx(0.0184)
+
+
+def test_algorithmic_bytes():
+    # Q, K, V read once, O written once (16 bits each) and the fp32 LSE
+    assert bench.algo_bytes(2, 16, 8192, 128) == 2 * 16 * 8192 * (3 * 2 * 128 + 2 * 128 + 4)
+    assert bench.algo_bytes(1, 1, 1, 64) == 8 * 64 + 4
+
+
+def test_parity_stats_flat_and_ulp_allowance():
+    ro = np.array([[0.5, 5.0], [-6.0, 1.0]])
+    rl = np.array([1.0, 2.0])
+    # bf16 at |x| in [4, 8): half an ulp is 2^-6; error 0.02 passes only with it
+    o = ro + np.array([[0.0, 0.02], [0.0, 0.0]])
+    st = bench.parity_stats(o, rl, ro, rl, "bf16")
+    assert st["pass"] and not st["flat_pass"] and st["n_pass_by_ulp_allowance"] == 1
+    assert st["max_abs_dO"] == pytest.approx(0.02)
+    # the same error where |O_ref| < 4 fails
+    o2 = ro + np.array([[0.02, 0.0], [0.0, 0.0]])
+    assert not bench.parity_stats(o2, rl, ro, rl, "bf16")["pass"]
+    # LSE outside 1e-3 fails; a NaN fails
+    assert not bench.parity_stats(ro, rl + 2e-3, ro, rl, "fp16")["pass"]
+    bad = ro.copy()
+    bad[0, 0] = np.nan
+    assert not bench.parity_stats(bad, rl, ro, rl, "fp16")["pass"]
+    both = bench.merge_parity([st, bench.parity_stats(ro, rl, ro, rl, "bf16")])
+    assert both["pass"] and both["rows"] == 4 and both["n_pass_by_ulp_allowance"] == 1
+
+
+def test_head_rows_cover_every_head():
+    B, H, S = 2, 16, 8192
+    rows = bench.head_rows(B, H, S, seed=1)
+    heads = rows // S
+    assert sorted(set(heads.tolist())) == list(range(B * H))
+    assert len(rows) == B * H * (16 + 8 + 16) and len(set(rows.tolist())) == len(rows)
+    r0 = rows[heads == 0] % S
+    assert set(range(16)) <= set(r0.tolist()) and set(range(S - 16, S)) <= set(r0.tolist())
+    small = bench.head_rows(1, 2, 20, seed=1)
+    assert len(small) == 40
+
+
+def test_per_config_workloads_are_the_named_sets():
+    got = {label: w for label, w in bench.per_config_workloads()}
+    assert (got["1"].S, got["1"].D, got["1"].dtype, got["1"].seed) == (128, 64, "fp16", 0)
+    assert (got["2"].B, got["2"].H, got["2"].S, got["2"].D, got["2"].seed) == (2, 16, 2048, 64, 1)
+    assert (got["3"].B, got["3"].H, got["3"].S, got["3"].D, got["3"].seed) == (1, 32, 2048, 128, 2)
+    assert got["4 Q,K x4"].qk_mult == 4.0 and got["4 Q,K x4"].seed == 3
+    for dt in ("fp16", "bf16"):
+        w = got[f"5 S8192 D64 {dt}"]
+        assert (w.S, w.D, w.dtype) == (8192, 64, dt) and w.causal == (False, True)

@@ -21,7 +21,9 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PKG = os.path.join(ROOT, "exact_attention_forward_10_gb300")
 
 # functions of bench.py allowed to import the oracle
-BENCH_ORACLE_USERS = {"cpu_oracle_run", "kv_oracle_run"}
+# the oracle leg of bench.py: the timed sample (self-attention and cache) and
+# the per-configuration comparison it runs after that sample
+BENCH_ORACLE_USERS = {"cpu_oracle_run", "kv_oracle_run", "per_config_parity"}
 
 
 def _files(top, exts):
