@@ -301,6 +301,34 @@ def copy_gbs(torch, dev, stream, src, dst, reps: int = 5) -> float:
     return nbytes / (best * 1e-3) / 1e9
 
 
+def copy_both_ms(torch, dev, h2d, d2h, reps: int = 5) -> float:
+    """Milliseconds for one host-to-device copy set (``h2d``: pairs (dst,
+    src)) and one device-to-host set (``d2h``) issued at the same time on
+    two streams, best of ``reps``: whether the two directions overlap."""
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    best = None
+    for _ in range(reps):
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b1 = torch.cuda.Event()
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(s1)
+        s2.wait_event(a)
+        with torch.cuda.stream(s1):
+            for d, x in h2d:
+                d.copy_(x, non_blocking=True)
+        with torch.cuda.stream(s2):
+            for d, x in d2h:
+                d.copy_(x, non_blocking=True)
+            b1.record(s2)
+        s1.wait_event(b1)
+        b.record(s1)
+        torch.cuda.synchronize(dev)
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    return best
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
 
@@ -626,8 +654,10 @@ def run_fattn(args):
     h2d_gbs = copy_gbs(torch, dev, stream, host, [q, k, v])
     d2h_gbs = copy_gbs(torch, dev, stream,
                        [t for c in MASKS for t in outs[c]], [t for c in MASKS for t in h_outs[c]])
+    both_ms = copy_both_ms(torch, dev, list(zip([q, k, v], host)),
+                           [(hh, d) for c in MASKS for hh, d in zip(h_outs[c], outs[c])])
     per_config, keep = [], []
-    if rank == 0:
+    if rank == 0 and not args.no_per_config:
         per_config, keep = run_per_config(torch, fattn, dev, stream, load_peaks(),
                                           main_x=x if world == 1 else None, main_w=w)
 
@@ -699,6 +729,7 @@ def run_fattn(args):
                     "schedule": E2E_SCHEDULE,
                     "h2d_gbs_alone": h2d_gbs, "d2h_gbs_alone": d2h_gbs,
                     "copy_floor_ms": max(h2d / h2d_gbs, d2h / d2h_gbs) / 1e6,
+                    "h2d_and_d2h_together_ms": both_ms,
                     "host_placement": placement,
                     "serial": {"value": world * flops_step / (e2e_serial_ms * 1e-3) / 1e12,
                                "ms_per_step": e2e_serial_ms}},
@@ -1381,6 +1412,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="fattn", choices=["fattn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-configuration block (e.g. for a profiler run)")
     ap.add_argument("--sweep", action="store_true",
                     help="TFLOPS over the sweep shapes, one JSON line each")
     ap.add_argument("--shape", default=None,

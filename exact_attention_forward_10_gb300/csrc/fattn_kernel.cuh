@@ -12,16 +12,22 @@
 // GB300 structure (one persistent CTA per SM):
 //   * QT query tiles of 128 rows per work unit share every K/V tile.
 //   * load warp:   TMA (128-byte swizzle) Q once per unit; K_j, V_j through an
-//                  NS-stage mbarrier ring.
-//   * MMA warp:    one thread issues tcgen05.mma: S_i = Q_i K_j^T into TMEM
-//                  (fp32, 128 lanes x 128 columns), then O_i += P_i V_j with
-//                  P_i read from TMEM and O_i kept in TMEM for the whole unit.
-//                  Head dim 128 (and 8-bit inputs): P_i overwrites S_i, the
-//                  two query tiles alternate (ping-pong).  Head dim 64: P_i
-//                  has its own columns, so scores run two key tiles ahead.
-//                  8-bit inputs: kind::f8f6f4 MMAs, P in E4M3, and P V in two
-//                  halves of the keys (the first half's MMAs overlap the
-//                  softmax of the second).
+//                  NS-stage mbarrier ring, in the order the MMAs use them.
+//   * MMA warps:   one thread of a warp issues tcgen05.mma: S_i = Q_i K_j^T
+//                  into TMEM (fp32, 128 lanes x 128 columns), then
+//                  O_i += P_i V_j with P_i read from TMEM and O_i kept in TMEM
+//                  for the whole unit.  16-bit inputs: P_i has 64 columns of
+//                  its own, so scores never wait for a P V, and two warps
+//                  issue (one the score MMAs, one the P V MMAs): a thread
+//                  that issues MMAs stalls until the pipe has nearly run the
+//                  ones before, so one warp's barrier waits would leave the
+//                  pipe idle.  Head dim 64: a score buffer per query tile.
+//                  Head dim 128: one score buffer that the two query tiles
+//                  fill in turn (TMEM: S 128, P 2 x 64, O 2 x 128 columns).
+//                  8-bit inputs: P_i overwrites S_i, the two query tiles
+//                  alternate (ping-pong), kind::f8f6f4 MMAs, P in E4M3, and
+//                  P V in two halves of the keys (the first half's MMAs
+//                  overlap the softmax of the second).
 //   * softmax warpgroup per query tile: thread r owns row r (TMEM lane r):
 //                  tcgen05.ld of its score row, mask, exp2 against a lazily
 //                  moved reference maximum with the scale folded into one
@@ -62,6 +68,14 @@
 // 1491 / 1412, so 16-bit inputs keep whole rows.
 #ifndef FATTN_HALF_PV
 #define FATTN_HALF_PV 1
+#endif
+
+// Head dim 128 with 16-bit inputs: both query tiles take turns in one TMEM
+// score buffer and each keeps its P in columns of its own (1: on), so the
+// scores of the next key tile never wait for the P V of this one; otherwise
+// P overwrites S in a score buffer per query tile.  A build-time choice.
+#ifndef FATTN_SHARED_S
+#define FATTN_SHARED_S 1
 #endif
 
 // Roles whose barrier waits spin instead of suspending (bit 0: load warp,
@@ -138,14 +152,28 @@ struct FwdLayout {
   // S_i(j+1) can be computed while the softmax of tile j still runs; else P_i
   // overwrites the first 64 columns of S_i.
   static constexpr bool kSepP = QT * (128 + 64) + QT * D <= (int)kTmemCols;
+  // TMEM columns of one query tile's P: 128 keys, two 16-bit or four 8-bit
+  // weights per column.
+  static constexpr int kPCols = 128 * EB / 4;
+  // Otherwise: one score buffer (columns 0-127) that the query tiles fill in
+  // turn, P_i in columns of its own, then the O_i.
+  static constexpr bool kShareS = !kSepP && EB == 2 && FATTN_SHARED_S != 0 &&
+                                  128 + QT * kPCols + QT * D <= (int)kTmemCols;
+  // With P in columns of its own, scores and P V depend on each other only
+  // through the softmax: one warp issues the score MMAs, another the P V
+  // MMAs, and each one's waits overlap the other's MMAs in the pipe.
+  static constexpr bool kDualMma = kSepP || kShareS;
   // P over S with 8-bit inputs: P V in two halves of the keys (FATTN_HALF_PV)
-  static constexpr bool kHalfPV = FATTN_HALF_PV != 0 && !kSepP && EB == 1;
-  __host__ __device__ static constexpr uint32_t colS(int i) { return 128u * i; }
+  static constexpr bool kHalfPV = FATTN_HALF_PV != 0 && !kSepP && !kShareS && EB == 1;
+  __host__ __device__ static constexpr uint32_t colS(int i) {
+    return kShareS ? 0u : 128u * i;
+  }
   __host__ __device__ static constexpr uint32_t colP(int i) {
-    return kSepP ? 128u * QT + 64u * i : colS(i);
+    return kSepP ? 128u * QT + 64u * i : kShareS ? 128u + (uint32_t)kPCols * i : colS(i);
   }
   __host__ __device__ static constexpr uint32_t colO(int i) {
-    return 128u * QT + (kSepP ? 64u * QT : 0u) + D * i;
+    return kShareS ? 128u + (uint32_t)kPCols * QT + D * i
+                   : 128u * QT + (kSepP ? 64u * QT : 0u) + D * i;
   }
   static_assert(colO(QT) <= kTmemCols, "TMEM budget");
 };
@@ -156,6 +184,7 @@ struct FwdWarps {
   static constexpr int kCorrection0 = 4 * QT;  // 4 warps
   static constexpr int kMma = 4 * QT + 4;
   static constexpr int kLoad = 4 * QT + 5;
+  static constexpr int kMma2 = 4 * QT + 6;  // P V issuer when S and P V issue apart
   static constexpr int kNumWarps = 4 * QT + 8;  // whole warpgroups
   static constexpr int kThreads = 32 * kNumWarps;
   // Registers per thread after the per-warpgroup split (QT == 2 only): the
@@ -352,7 +381,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       ptx::mbar_init(bar(L::bKVFull + s), 1);
       ptx::mbar_init(bar(L::bKVEmpty + s), 1);
     }
-    ptx::mbar_init(bar(L::bDrain), 1);
+    ptx::mbar_init(bar(L::bDrain), L::kDualMma ? 2 : 1);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -403,9 +432,28 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                              c * L::kChunkCols, w.q_row0 + kBM * i, w.bh);
           ++q_uses[i];
         }
-        for (int j = 0; ok && j < w.n_max; ++j) {
-#pragma unroll
-          for (int kv = 0; kv < 2; ++kv) {
+        // Items in the order the MMA warps consume them: K_j, V_j; when
+        // scores and P V issue apart, K_0, then K_{j+1} before V_j (the next
+        // tile's scores are issued while this tile's softmax runs), so the
+        // slots are released about in load order.
+        for (int it = 0; ok && it < 2 * w.n_max; ++it) {
+          int j, kv;
+          if constexpr (L::kDualMma) {
+            if (it == 0) {
+              j = 0;
+              kv = 0;
+            } else if (it == 2 * w.n_max - 1) {
+              j = w.n_max - 1;
+              kv = 1;
+            } else {
+              j = (it - 1) / 2 + ((it & 1) ? 1 : 0);
+              kv = (it & 1) ? 0 : 1;
+            }
+          } else {
+            j = it / 2;
+            kv = it & 1;
+          }
+          {
             if (kv == 1) FATTN_TRACE_EV(k, j, 7);
             if (!ptx::mbar_wait<kSpinLoad>(bar(L::bKVEmpty + kv_idx), kv_ph ^ 1u, abort_flag, tmo)) {
               raise_error(p, abort_flag, kErrPipelineTimeout, kRoleLoad, L::bKVEmpty + kv_idx);
@@ -437,20 +485,24 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         if (q_uses[i] > 0)
           ptx::mbar_wait_drain(bar(L::bQFull + i), (q_uses[i] - 1) & 1, tmo);
     }
-  } else if (warp == W::kMma) {
-    // ------------------------------------------------------------- MMA warp
-    // The whole warp runs this role converged, so its counters and
-    // descriptors stay warp-uniform; one elected lane issues each tcgen05
-    // instruction.  The issuing thread stalls until the tensor pipe accepts
-    // an MMA, so everything it does between two MMA groups is tensor idle
-    // time: that path is kept short.
+  } else if (warp == W::kMma || (L::kDualMma && warp == W::kMma2)) {
+    // ------------------------------------------------------------ MMA warps
+    // Each MMA warp runs its role converged, so its counters and descriptors
+    // stay warp-uniform; one elected lane issues each tcgen05 instruction.
+    // The issuing thread stalls until the tensor pipe has nearly finished
+    // the MMAs before, so what one warp does between two MMA groups (barrier
+    // waits, commits) is tensor idle time unless another warp's MMAs are
+    // queued meanwhile: with P in columns of its own, warp kMma issues the
+    // score MMAs and warp kMma2 the P V MMAs.
+    const bool s_role = warp == W::kMma;  // dual issue: this warp's share
     {
       constexpr uint32_t kIdS = FP8 ? ptx::idesc_e4m3(kBM, kBN, 0, 0)
                                     : ptx::idesc_f16(BF16 ? 1 : 0, kBM, kBN, 0, 0);
       constexpr uint32_t kIdPV = FP8 ? ptx::idesc_e4m3(kBM, D, 0, 1)
                                      : ptx::idesc_f16(BF16 ? 1 : 0, kBM, D, 0, 1);
       uint32_t kv_idx = 0, kv_ph = 0;
-      uint32_t kv_item = 0;  // separate-P layout: ring index of the next unit's K_0
+      uint32_t kv_item = 0;  // separate-P layouts: ring index of the next unit's K_0
+      uint32_t s_total = 0;  // shared score buffer: S MMAs issued into it so far
       int q_uses[QT], p_cnt[QT], oe_cnt[QT], used[QT], s_issued[QT];
       for (int i = 0; i < QT; ++i) q_uses[i] = p_cnt[i] = oe_cnt[i] = used[i] = s_issued[i] = 0;
       bool ok = true;
@@ -526,21 +578,17 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         if (t >= p.total_units) continue;
         int n[QT];
         const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
-        for (int i = 0; ok && i < QT; ++i)
-          if (n[i] > 0) {
-            ok = wait_or_fail(L::bQFull + i, q_uses[i] & 1);
-            ++q_uses[i];
-          }
+        if (!L::kDualMma || s_role)
+          for (int i = 0; ok && i < QT; ++i)
+            if (n[i] > 0) {
+              ok = wait_or_fail(L::bQFull + i, q_uses[i] & 1);
+              ++q_uses[i];
+            }
         if (!ok) break;
-        if constexpr (L::kSepP) {
-          // Separate P: S_i(j+2) needs only that the softmax has read
-          // S_i(j+1) (s_free), so each tile's scores are two steps ahead and
-          // the two softmax warpgroups run back to back.  Per step j the
-          // order is PV_0(j), S_0(j+2), PV_1(j), S_1(j+2).  K/V items are
-          // then taken slightly out of ring order (K_{j+2} before V_{j+1}),
-          // so each is addressed by its index in the ring; the reordering
-          // window (two items) is far below the ring depth.
-          static_assert(NS >= 6, "separate-P issue order needs a deeper K/V ring");
+        if constexpr (L::kDualMma) {
+          // K/V items in the load warp's order K_0, K_1, V_0, K_2, V_1, ...,
+          // V_{n-1} (K_{j+1} before V_j: scores run ahead of P V), addressed
+          // by their index in the ring.
           const uint32_t base = kv_item;  // ring index of this unit's K_0
           kv_item += 2u * (uint32_t)w.n_max;
           auto wait_item = [&](uint32_t idx) -> bool {
@@ -550,16 +598,9 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
             return true;
           };
           auto item_slot = [&](uint32_t idx) -> int { return (int)((base + idx) % NS); };
-          auto issue_s_step = [&](int i, int jj) -> bool {
-            if (s_issued[i] > 0 && !wait_or_fail(L::bSFree + i, (s_issued[i] - 1) & 1))
-              return false;
-            ++s_issued[i];
-            ptx::tc_fence_after();
-            FATTN_TRACE_EV(k, jj, 26 + 2 * i);
-            issue_s(i, (uint32_t)item_slot(2u * jj));
-            commit(L::bSFull + i);
-            if (jj == n[i] - 1) commit(L::bQEmpty + i);
-            return true;
+          auto k_item = [&](int jj) -> uint32_t { return jj == 0 ? 0u : 2u * jj - 1u; };
+          auto v_item = [&](int jj) -> uint32_t {
+            return jj < w.n_max - 1 ? 2u * jj + 2u : 2u * jj + 1u;
           };
           auto last_user = [&](int jj) -> int {
             int u = -1;
@@ -567,24 +608,44 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
               if (jj < n[i]) u = i;
             return u;
           };
-          // prologue: S_i(0) and S_i(1)
-          for (int jj = 0; ok && jj < 2 && jj < w.n_max; ++jj) {
-            ok = wait_item(2u * jj);
-            for (int i = 0; ok && i < QT; ++i)
-              if (jj < n[i]) ok = issue_s_step(i, jj);
-            if (ok) commit(L::bKVEmpty + item_slot(2u * jj));
-          }
-          for (int j = 0; ok && j < w.n_max; ++j) {
-            if (!wait_item(2u * j + 1u)) {
-              ok = false;
-              break;
+          if (s_role) {
+            // S_0(j), S_1(j), S_0(j+1), ...: each waits until its score
+            // buffer's previous contents are in the softmax's registers
+            // (per tile, or for the shared buffer the other tile's).
+            for (int j = 0; ok && j < w.n_max; ++j) {
+              if (!wait_item(k_item(j))) {
+                ok = false;
+                break;
+              }
+              for (int i = 0; ok && i < QT; ++i) {
+                if (j >= n[i]) continue;
+                if constexpr (L::kShareS) {
+                  if (s_total > 0) ok = wait_or_fail(L::bSFree, (s_total - 1) & 1u);
+                  ++s_total;
+                } else {
+                  if (s_issued[i] > 0) ok = wait_or_fail(L::bSFree + i, (s_issued[i] - 1) & 1);
+                  ++s_issued[i];
+                }
+                if (!ok) break;
+                ptx::tc_fence_after();
+                FATTN_TRACE_EV(k, j, 26 + 2 * i);
+                issue_s(i, (uint32_t)item_slot(k_item(j)));
+                commit(L::bSFull + i);
+                if (j == n[i] - 1) commit(L::bQEmpty + i);
+                if (i == last_user(j)) commit(L::bKVEmpty + item_slot(k_item(j)));
+              }
             }
-            FATTN_TRACE_EV(k, j, 24);
-            const int last_v = last_user(j);
-            const int last_k = last_user(j + 2);
-            bool have_k = false;
-            for (int i = 0; ok && i < QT; ++i) {
-              if (j < n[i]) {
+          } else {
+            // PV_0(j), PV_1(j), ...: each waits for its P (and, first in a
+            // unit, for the epilogue to have read the previous unit's O).
+            for (int j = 0; ok && j < w.n_max; ++j) {
+              if (!wait_item(v_item(j))) {
+                ok = false;
+                break;
+              }
+              FATTN_TRACE_EV(k, j, 24);
+              for (int i = 0; ok && i < QT; ++i) {
+                if (j >= n[i]) continue;
                 ok = wait_or_fail(L::bPFull + i, p_cnt[i] & 1);
                 ++p_cnt[i];
                 if (ok && j == 0 && used[i] > 0) {
@@ -594,20 +655,9 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                 if (!ok) break;
                 FATTN_TRACE_EV(k, j, 25 + 2 * i);
                 ptx::tc_fence_after();
-                issue_pv(i, (uint32_t)item_slot(2u * j + 1u), j > 0);
+                issue_pv(i, (uint32_t)item_slot(v_item(j)), j > 0);
                 commit(L::bPVDone + i);
-                if (i == last_v) commit(L::bKVEmpty + item_slot(2u * j + 1u));
-              }
-              if (j + 2 < n[i]) {
-                if (!have_k) {
-                  if (!wait_item(2u * (j + 2))) {
-                    ok = false;
-                    break;
-                  }
-                  have_k = true;
-                }
-                ok = issue_s_step(i, j + 2);
-                if (ok && i == last_k) commit(L::bKVEmpty + item_slot(2u * (j + 2)));
+                if (i == last_user(j)) commit(L::bKVEmpty + item_slot(v_item(j)));
               }
             }
           }
@@ -690,7 +740,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         for (int i = 0; i < QT; ++i)
           if (n[i] > 0) ++used[i];
       }
-      // Drain: every MMA this warp issued completes before TMEM is freed.
+      // Drain: every MMA these warps issued completes before TMEM is freed.
       commit(L::bDrain);
       ptx::mbar_wait_drain(bar(L::bDrain), 0, tmo);
     }
@@ -845,10 +895,11 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           for (int e = 0; e < 32; ++e) s[ch * 32 + e] = __uint_as_float(u[e]);
         }
         ptx::tmem_wait_ld();
-        if constexpr (L::kSepP) {
-          // S_i is in registers: the MMA may compute S_i(j+1) into it now.
+        if constexpr (L::kSepP || L::kShareS) {
+          // S_i is in registers: the MMA may compute the next scores into
+          // this buffer now (S_i(j+1); in the shared buffer, the other tile's).
           ptx::tc_fence_before();
-          ptx::mbar_arrive(bar(L::bSFree + i));
+          ptx::mbar_arrive(bar(L::bSFree + (L::kShareS ? 0 : i)));
         }
         FATTN_TRACE_EV(k, j, 8 * i + 2);
         // masks: causal diagonal tile keeps key <= query; keys >= S removed
@@ -863,7 +914,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           for (int e = 0; e < kBN; ++e) s[e] = e < limit ? s[e] : -INFINITY;
         }
         float m_use = m, alpha = 1.0f, sum, tmax, rsum = 0.f;
-        if constexpr (L::kSepP) {
+        if constexpr (L::kSepP || L::kShareS) {
           // Separate P: the maximum first (no redo is possible once packed P
           // waits in registers for its buffer), then the exponents.
           float acc[8];
