@@ -16,23 +16,19 @@
 //   * MMA warps:   one thread of a warp issues tcgen05.mma: S_i = Q_i K_j^T
 //                  into TMEM (fp32, 128 lanes x 128 columns), then
 //                  O_i += P_i V_j with P_i read from TMEM and O_i kept in TMEM
-//                  for the whole unit.  16-bit inputs: P_i has 64 columns of
-//                  its own, so scores never wait for a P V, and two warps
-//                  issue (one the score MMAs, one the P V MMAs): a thread
-//                  that issues MMAs stalls until the pipe has nearly run the
-//                  ones before, so one warp's barrier waits would leave the
-//                  pipe idle.  Head dim 64: a score buffer per query tile.
-//                  Head dim 128: one score buffer that the two query tiles
-//                  fill in turn (TMEM: S 128, P 2 x 64, O 2 x 128 columns).
-//                  8-bit inputs: P_i overwrites S_i, the two query tiles
-//                  alternate (ping-pong), kind::f8f6f4 MMAs, P in E4M3, and
-//                  P V in two halves of the keys (the first half's MMAs
-//                  overlap the softmax of the second).
+//                  for the whole unit.  One score buffer that the two query
+//                  tiles fill in turn and P_i in columns of its own (TMEM:
+//                  S 128, P 2 x 64 (16-bit) or 2 x 32 (E4M3), O 2 x D), so
+//                  scores never wait for a P V; two warps issue, one the
+//                  score MMAs and one the P V MMAs: a thread that issues MMAs
+//                  stalls until the pipe has nearly run the ones before, so
+//                  one warp's barrier waits would leave the pipe idle.  8-bit
+//                  inputs: kind::f8f6f4 MMAs and P in E4M3.
 //   * softmax warpgroup per query tile: thread r owns row r (TMEM lane r):
 //                  tcgen05.ld of its score row, mask, exp2 against a lazily
 //                  moved reference maximum with the scale folded into one
-//                  FFMA, row sums, P back to TMEM; when a row's reference
-//                  moves, the same warp rescales that row of O_i in TMEM.
+//                  FFMA, row sums, P to TMEM; when a row's reference moves,
+//                  the same warp rescales that row of O_i in TMEM.
 //                  (m, l) live in registers; no shuffles are needed because a
 //                  row never leaves its thread.
 //   * epilogue warpgroup: one 1/l per row, cast to 16-bit, vector stores of
@@ -61,21 +57,33 @@
 #endif
 
 // P V issued in two halves of the keys (the first half while the softmax
-// still works on the second) for 8-bit inputs, where P overwrites S; a
-// build-time choice (1: on).  Measured on the B2 H16 S8192 D128 workloads:
-// E4M3 1436 / 1367 TF against 1292 / 1247 in whole rows (the softmax is
-// longer and P V shorter than with 16-bit inputs); bf16 1335 / 1278 against
-// 1491 / 1412, so 16-bit inputs keep whole rows.
+// still works on the second) when P overwrites S (FATTN_SHARED_S 0) with
+// 8-bit inputs; a build-time choice (1: on).  Measured in that layout on the
+// B2 H16 S8192 D128 workloads: E4M3 1436 / 1367 TF against 1292 / 1247 in
+// whole rows; bf16 1335 / 1278 against 1491 / 1412, so 16-bit inputs keep
+// whole rows.
 #ifndef FATTN_HALF_PV
 #define FATTN_HALF_PV 1
 #endif
 
-// Head dim 128 with 16-bit inputs: both query tiles take turns in one TMEM
-// score buffer and each keeps its P in columns of its own (1: on), so the
-// scores of the next key tile never wait for the P V of this one; otherwise
-// P overwrites S in a score buffer per query tile.  A build-time choice.
+// Head dim 128: both query tiles take turns in one TMEM score buffer and
+// each keeps its P in columns of its own (1: on), so the scores of the next
+// key tile never wait for the P V of this one; otherwise (0) P overwrites S
+// in a score buffer per query tile and one warp issues all MMAs.  A
+// build-time choice; measured on one GB300, B2 H16 S8192: bf16 1622-1625 /
+// 1545-1550 TF (maximum first) and 1766-1777 / 1550-1608 (fused) against
+// 1525 / 1419-1428, E4M3 1850 / 1780-1790 against 1429 / 1355.
 #ifndef FATTN_SHARED_S
 #define FATTN_SHARED_S 1
+#endif
+
+// Head dim 64: a score buffer per query tile (1) or the shared buffer of
+// head dim 128 (0, default: the tiles' softmax warpgroups then alternate
+// instead of running side by side, and one's waits overlap the other's
+// exponents; B2 H16 S8192 bf16 1110 / 1072 TF against 1002 / 958); a
+// build-time choice.
+#ifndef FATTN_D64_SCORE_PER_TILE
+#define FATTN_D64_SCORE_PER_TILE 0
 #endif
 
 // Roles whose barrier waits spin instead of suspending (bit 0: load warp,
@@ -151,18 +159,20 @@ struct FwdLayout {
   // TMEM columns.  When they fit (D = 64), P_i gets its own 64 columns, so
   // S_i(j+1) can be computed while the softmax of tile j still runs; else P_i
   // overwrites the first 64 columns of S_i.
-  static constexpr bool kSepP = QT * (128 + 64) + QT * D <= (int)kTmemCols;
+  static constexpr bool kSepP = FATTN_D64_SCORE_PER_TILE != 0 &&
+                                QT * (128 + 64) + QT * D <= (int)kTmemCols;
   // TMEM columns of one query tile's P: 128 keys, two 16-bit or four 8-bit
   // weights per column.
   static constexpr int kPCols = 128 * EB / 4;
   // Otherwise: one score buffer (columns 0-127) that the query tiles fill in
   // turn, P_i in columns of its own, then the O_i.
-  static constexpr bool kShareS = !kSepP && EB == 2 && FATTN_SHARED_S != 0 &&
+  static constexpr bool kShareS = !kSepP && FATTN_SHARED_S != 0 &&
                                   128 + QT * kPCols + QT * D <= (int)kTmemCols;
   // With P in columns of its own, scores and P V depend on each other only
   // through the softmax: one warp issues the score MMAs, another the P V
   // MMAs, and each one's waits overlap the other's MMAs in the pipe.
   static constexpr bool kDualMma = kSepP || kShareS;
+
   // P over S with 8-bit inputs: P V in two halves of the keys (FATTN_HALF_PV)
   static constexpr bool kHalfPV = FATTN_HALF_PV != 0 && !kSepP && !kShareS && EB == 1;
   __host__ __device__ static constexpr uint32_t colS(int i) {
@@ -860,6 +870,31 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       const float2 s4 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
       return s4.x + s4.y;
     };
+    // The 8-bit form: four E4M3 weights per word (byte j = key 4e + j), and
+    // the sum of the weights as rounded (rsum), the normaliser of O.
+    auto exp_pack8 = [&](const float (&s)[kBN], float mref, uint32_t (&pk)[kBN / 4],
+                         float& rsum) -> float {
+      const float2 c2 = make_float2(c, c);
+      const float2 neg2 = make_float2(-mref, -mref);
+      float2 sum2[4];
+      float r0 = 0.f, r1 = 0.f;
+#pragma unroll
+      for (int a = 0; a < 4; ++a) sum2[a] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int e = 0; e < kBN / 4; ++e) {
+        const float2 x0 = __ffma2_rn(make_float2(s[4 * e], s[4 * e + 1]), c2, neg2);
+        const float2 x1 = __ffma2_rn(make_float2(s[4 * e + 2], s[4 * e + 3]), c2, neg2);
+        const float2 p0 = make_float2(ex2(x0.x), ex2(x0.y));
+        const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+        sum2[(2 * e) & 3] = __fadd2_rn(sum2[(2 * e) & 3], p0);
+        sum2[(2 * e + 1) & 3] = __fadd2_rn(sum2[(2 * e + 1) & 3], p1);
+        pk[e] = pack4_e4m3(p0.x, p0.y, p1.x, p1.y);
+        add4_e4m3(pk[e], r0, r1);
+      }
+      rsum = r0 + r1;
+      const float2 s4 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
+      return s4.x + s4.y;
+    };
     for (int k = 0; k * (int)gridDim.x < p.total_units; ++k) {
       const int t = unit_of_round(k);
       if (t >= p.total_units) continue;
@@ -915,8 +950,15 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         }
         float m_use = m, alpha = 1.0f, sum, tmax, rsum = 0.f;
         if constexpr (L::kSepP || L::kShareS) {
-          // Separate P: the maximum first (no redo is possible once packed P
-          // waits in registers for its buffer), then the exponents.
+          // Separate P, maximum first: the exponents go to registers at once
+          // and P to TMEM once the previous P V has landed (no redo is
+          // possible once packed P waits in registers for its buffer).
+          // Waiting for that P V first and exponentiating against the
+          // current reference with the maximum on the side (as P over S
+          // does) saves the maximum pass, but measured slower on scores that
+          // spread widely (Q, K x 4: 1190 against 1617-1667 TF at B2 H16
+          // S8192 D128, a redo in nearly every tile) and for causal masks,
+          // and within 1-9% faster only at head dim 128 on N(0,1) inputs.
           float acc[8];
 #pragma unroll
           for (int a = 0; a < 8; ++a) acc[a] = fmax3(s[2 * a], s[2 * a + 1], -INFINITY);
@@ -933,8 +975,11 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           if (m_use == -INFINITY) m_use = 0.f;  // no allowed key in this row yet
           if (move && j > 0) alpha = ex2(m - m_use);
           FATTN_TRACE_EV(k, j, 8 * i + 3);
-          uint32_t pk[kBN / 2];
-          sum = exp_pack(s, m_use, pk);
+          uint32_t pk[FP8 ? kBN / 4 : kBN / 2];
+          if constexpr (FP8)
+            sum = exp_pack8(s, m_use, pk, rsum);
+          else
+            sum = exp_pack(s, m_use, pk);
           // P_i is free once the PV that read its previous contents is done
           // (that PV also ends the last update of O_i before a rescale).
           if (p_writes > 0) {
@@ -948,7 +993,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           }
           ++p_writes;
 #pragma unroll
-          for (int ch = 0; ch < kBN / 32; ++ch) {
+          for (int ch = 0; ch < (FP8 ? kBN / 64 : kBN / 32); ++ch) {
             uint32_t part[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e) part[e] = pk[ch * 16 + e];
@@ -1052,13 +1097,14 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           l += sum1;
           lr += FP8 ? rsum1 : sum1 + round_corr(tmax1, m);
         } else {
-          // Reference maximum m (log2 domain).  The first tile of a row has
-          // none yet: take its maximum first.  Later tiles exponentiate against
-          // the current reference at once and track their maximum on the side;
-          // the rare tile whose maximum passes the reference by more than
-          // kRescaleLog2 is redone against the new maximum (warp-uniformly,
-          // since P goes back to TMEM with warp-wide stores).  O, l and the
-          // exponent share the reference, so any choice is exact; p <= 2^8.
+          // P over S.  Reference maximum m (log2 domain).  The first tile of
+          // a row has none yet: take its maximum first.  Later tiles
+          // exponentiate against the current reference at once and track
+          // their maximum on the side; the rare tile whose maximum passes the
+          // reference by more than kRescaleLog2 is redone against the new
+          // maximum (warp-uniformly, since P goes back to TMEM with warp-wide
+          // stores).  O, l and the exponent share the reference, so any
+          // choice is exact; p <= 2^8.
           if (j == 0) {
             float acc[8];
 #pragma unroll
