@@ -50,7 +50,8 @@
 
 // Optional timeline hook: FATTN_TRACE_EV(round, kv_tile, event) records one
 // event of the pipeline when an instrumented build defines it; the product
-// build compiles it to nothing.
+// build compiles it to nothing.  Events of a whole unit use the key-tile
+// slot kTraceUnit.
 #ifndef FATTN_TRACE_EV
 #define FATTN_TRACE_INIT ((void)0)
 #define FATTN_TRACE_EV(round, kv_tile, event) ((void)0)
@@ -95,6 +96,7 @@
 
 namespace fattn {
 
+constexpr int kTraceUnit = 71;
 constexpr bool kSpinLoad = (FATTN_SPIN_ROLES & 1) != 0;
 constexpr bool kSpinMma = (FATTN_SPIN_ROLES & 2) != 0;
 constexpr bool kSpinSoftmax = (FATTN_SPIN_ROLES & 4) != 0;
@@ -435,6 +437,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
             break;
           }
           const uint32_t qb = bar(L::bQFull + i);
+          FATTN_TRACE_EV(k, kTraceUnit, 13 + i);
           ptx::mbar_arrive_expect_tx(qb, L::kTileBytes);
 #pragma unroll
           for (int c = 0; c < L::kChunks; ++c)
@@ -593,6 +596,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
             if (n[i] > 0) {
               ok = wait_or_fail(L::bQFull + i, q_uses[i] & 1);
               ++q_uses[i];
+              FATTN_TRACE_EV(k, kTraceUnit, 15 + i);
             }
         if (!ok) break;
         if constexpr (L::kDualMma) {
@@ -661,6 +665,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                 if (ok && j == 0 && used[i] > 0) {
                   ok = wait_or_fail(L::bOEmpty + i, oe_cnt[i] & 1);
                   ++oe_cnt[i];
+                  FATTN_TRACE_EV(k, kTraceUnit, 21 + i);
                 }
                 if (!ok) break;
                 FATTN_TRACE_EV(k, j, 25 + 2 * i);
@@ -1209,6 +1214,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         const float lse = sRowM[i * kBM + r];  // log-sum-exp of the row
         if (!wait_all(L::bPVDone + i, (uint32_t)(pv_base[i] + n[i] - 1) & 1u)) { ok = false; break; }
         pv_base[i] += n[i];
+        FATTN_TRACE_EV(k, kTraceUnit, 17 + i);
         ptx::tc_fence_after();
         const float inv_l = p.o_scale / l;
         const int row = w.q_row0 + kBM * i + r;
@@ -1217,25 +1223,43 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         uint4* const orow = reinterpret_cast<uint4*>(
             reinterpret_cast<uint8_t*>(p.o) + grow * (size_t)(D * 2));
         const uint32_t o_addr = tmem + lane_off + L::colO(i);
+        const bool o_aligned32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t u[32];
           ptx::tmem_ld32(o_addr + ch * 32, u);
           ptx::tmem_wait_ld();
+          if (ch == D / 32 - 1) {
+            // O_i (and the row statistics, read above) are in registers: the
+            // next unit's P V may overwrite them while the stores below run.
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(L::bOEmpty + i));
+            FATTN_TRACE_EV(k, kTraceUnit, 19 + i);
+          }
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             pk[e] = pack2<BF16>(__uint_as_float(u[2 * e]) * inv_l,
                                 __uint_as_float(u[2 * e + 1]) * inv_l);
           if (valid) {
+            // a thread writes its own row: 32-byte stores when the output is
+            // 32-byte aligned (rows are 128 or 256 bytes), else 16-byte ones
+            if (o_aligned32) {
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              orow[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+              for (int v8 = 0; v8 < 2; ++v8) {
+                uint32_t w8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) w8[e] = pk[8 * v8 + e];
+                ptx::st_global_v8(orow + ch * 4 + 2 * v8, w8);
+              }
+            } else {
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4)
+                orow[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+            }
           }
         }
         if (valid) p.lse[grow] = lse;
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::bOEmpty + i));
       }
     }
   }

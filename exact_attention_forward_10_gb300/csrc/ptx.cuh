@@ -171,6 +171,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// 32 bytes to global memory in one instruction; ``p`` must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // ------------------------------------------------------------------- tcgen05
 
 // Allocate ``ncols`` TMEM columns (power of two >= 32); the base address is

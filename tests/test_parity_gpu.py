@@ -150,3 +150,38 @@ def test_repeated_calls_are_deterministic():
     o2, l2 = run_cuda(x, True)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("offset_bytes", [0, 16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_output_alignment(D, offset_bytes):
+    """O (and the LSE) at a 32-byte boundary and 16 bytes past one: the
+    epilogue's two store widths give the same result as the oracle."""
+    import math
+
+    import torch
+
+    import exact_attention_forward_10_gb300 as fattn
+    import oracle
+
+    x = attn_inputs.make_qkv(1, 4, 300, D, "bf16", seed=1300 + D)
+    dev = torch.device("cuda:0")
+    q, k, v = (torch.from_numpy(a).to(dev).to(torch.bfloat16) for a in (x.q, x.k, x.v))
+    n = q.numel()
+    ob = torch.full((n + 64,), float("nan"), dtype=torch.bfloat16, device=dev)
+    base = ob.data_ptr()
+    skip = ((-base) % 32 + offset_bytes) // 2  # elements to a 32-byte boundary, then the offset
+    o = ob[skip:skip + n].view(q.shape)
+    assert (o.data_ptr() % 32) == offset_bytes
+    lse = torch.full((1, 4, 300), float("nan"), dtype=torch.float32, device=dev)
+    for causal in (False, True):
+        rc = fattn.fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                             1, 4, 300, D, causal, 1.0 / math.sqrt(D), fattn.FATTN_BF16, 0)
+        assert rc == 0
+        torch.cuda.synchronize()
+        assert fattn.fattn_last_error(0)[0] == 0
+        ro, rl = oracle.attn_fwd(x.q, x.k, x.v, causal, 1.0 / math.sqrt(D))
+        compare(o.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, "bf16",
+                f"D{D} offset {offset_bytes} causal={causal}")
+        # the guard elements around O were not written
+        assert torch.isnan(ob[:skip]).all() and torch.isnan(ob[skip + n:]).all()
