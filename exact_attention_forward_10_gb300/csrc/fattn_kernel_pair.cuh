@@ -100,9 +100,9 @@ struct PairWarps {
   static constexpr int kThreads = 32 * kNumWarps;
   // 384 threads launch with 168 registers each; the per-warpgroup split
   // adds up to the same total.
-  static constexpr int kRegSoftmax = 240;
-  static constexpr int kRegEpilogue = 136;
-  static constexpr int kRegOther = 128;
+  static constexpr int kRegSoftmax = 200;
+  static constexpr int kRegEpilogue = 152;
+  static constexpr int kRegOther = 152;
   static_assert(kRegSoftmax + kRegEpilogue + kRegOther == 3 * 168,
                 "register split must equal the launch allocation");
 };
@@ -247,6 +247,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
           ok = false;
           break;
         }
+        FATTN_TRACE_EV(k, kTraceUnit, 0);
         if (leader) ptx::mbar_arrive_expect_tx(bar(L::bQFull), 2 * kQBytes);
 #pragma unroll
         for (int c = 0; c < D / kSwizzleChunkCols; ++c)
@@ -278,6 +279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
                                       (D / 2) * (int)rank + c * kSwizzleChunkCols, j * kBN,
                                       w.bh);
             }
+            FATTN_TRACE_EV(k, j, 1 + kv);
             filled |= 1u << idx;
             fill_ph = (fill_ph & ~(1u << idx)) | (ph << idx);
             if (++idx == NS) {
@@ -309,7 +311,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
       const uint32_t k_lo = ptx::desc_sw128_lo(sKV, 16);
       const uint32_t v_lo = ptx::desc_sw128_lo(sKV, kVChunk);  // LBO: next 64 columns
       uint32_t item = 0;  // ring index of the next unit's K_0
-      int q_uses = 0, pf_cnt[NSB] = {}, oe_cnt = 0, used = 0;
+      int q_uses = 0, oe_cnt = 0, used = 0;
+      uint32_t pf_par = 0;  // bit b: parity of buffer b's P-full completions seen
       bool ok = true;
       auto wait_or_fail = [&](int slot, uint32_t parity) -> bool {
         bool w_ok = ptx::mbar_wait_cluster(bar(slot), parity, abort_flag, tmo);
@@ -366,6 +369,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
         };
         auto slot_of = [&](uint32_t i) -> uint32_t { return (ubase + i) % NS; };
         if (!wait_or_fail(L::bQFull, q_uses & 1)) break;
+        FATTN_TRACE_EV(k, kTraceUnit, 4);
         ++q_uses;
         ptx::tc_fence_after();
         // prologue: S(0) .. S(NSB-1)
@@ -373,6 +377,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
           ok = wait_item(2u * j);
           if (!ok) break;
           issue_s(j, slot_of(2u * j));
+          FATTN_TRACE_EV(k, j, 5);
           commit(L::bSFull + j);
           commit(L::bKVEmpty + (int)slot_of(2u * j));
           if (j == w.n - 1) commit(L::bQEmpty);
@@ -380,14 +385,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
         for (int j = 0; ok && j < w.n; ++j) {
           const int b = j % NSB;
           if (!wait_item(2u * j + 1u)) { ok = false; break; }
-          if (!wait_or_fail(L::bPFull + b, pf_cnt[b] & 1)) { ok = false; break; }
-          ++pf_cnt[b];
+          if (!wait_or_fail(L::bPFull + b, (pf_par >> b) & 1u)) { ok = false; break; }
+          FATTN_TRACE_EV(k, j, 7);
+          pf_par ^= 1u << b;
           if (j == 0 && used > 0) {
             if (!wait_or_fail(L::bOEmpty, oe_cnt & 1)) { ok = false; break; }
+            FATTN_TRACE_EV(k, kTraceUnit, 8);
             ++oe_cnt;
           }
           ptx::tc_fence_after();
           issue_pv(b, slot_of(2u * j + 1u), j > 0);
+          FATTN_TRACE_EV(k, j, 6);
           commit(L::bPVDone + b);
           commit(L::bKVEmpty + (int)slot_of(2u * j + 1u));
           if (j == w.n - 1) commit(L::bODone);
@@ -396,6 +404,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
           if (j + NSB < w.n) {
             if (!wait_item(2u * (j + NSB))) { ok = false; break; }
             issue_s(b, slot_of(2u * (j + NSB)));
+            FATTN_TRACE_EV(k, j + NSB, 5);
             commit(L::bSFull + b);
             commit(L::bKVEmpty + (int)slot_of(2u * (j + NSB)));
             if (j + NSB == w.n - 1) commit(L::bQEmpty);
@@ -415,8 +424,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float c = p.scale_log2;
-    int sf_cnt[NSB] = {};
-    int pv_cnt[NSB] = {};  // P V MMAs reading each buffer, issued so far
+    // Per score buffer, the parity of its S-full completions seen so far and
+    // of the P V MMAs reading it issued so far (bit b: buffer b).  Bit masks,
+    // not arrays: a buffer index that varies at run time would put an array
+    // in local memory.
+    uint32_t sf_par = 0, pv_par = 0;
     int units_done = 0;
     bool ok = true;
     auto wait_all = [&](int slot, uint32_t parity) -> bool {
@@ -466,8 +478,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
       float m = -INFINITY, l = 0.f, lr = 0.f;
       for (int j = 0; j < w.n; ++j) {
         const int b = j % NSB;
-        if (!wait_all(L::bSFull + b, sf_cnt[b] & 1)) { ok = false; break; }
-        ++sf_cnt[b];
+        if (!wait_all(L::bSFull + b, (sf_par >> b) & 1u)) { ok = false; break; }
+        if (quarter == 0) FATTN_TRACE_EV(k, j, 10);
+        sf_par ^= 1u << b;
         ptx::tc_fence_after();
         const uint32_t s_addr = tmem + lane_off + L::colS(b);
         float s[kBN];
@@ -517,6 +530,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
               alpha = ex2(m - m_use);
             }
             sum = exp_pass(s, m_use, s_addr, std::false_type{}, tmax);
+            if (quarter == 0) FATTN_TRACE_EV(k, j, 13);
           }
         }
         // A row that moved its reference scales its O rows, once the P V of
@@ -526,8 +540,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
         // older than S(j)), so its parity is unambiguous.
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
           const int pb = (j - 1) % NSB;
-          if (!wait_all(L::bPVDone + pb, (uint32_t)(pv_cnt[pb] - 1) & 1u)) { ok = false; break; }
+          if (!wait_all(L::bPVDone + pb, ((pv_par >> pb) & 1u) ^ 1u)) { ok = false; break; }
           ptx::tc_fence_after();
+          if (quarter == 0) FATTN_TRACE_EV(k, j, 14);
           const uint32_t o_addr = tmem + lane_off + L::kColO;
 #pragma unroll 1
           for (int ch = 0; ch < D / 32; ++ch) {
@@ -544,13 +559,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
         __syncwarp();
         // rank 0 arrives on its own barrier (CTA scope); the peer's warps
         // release across the cluster.
+        if (quarter == 0) FATTN_TRACE_EV(k, j, 11);
         if (lane == 0) {
           if (leader)
             ptx::mbar_arrive(bar(L::bPFull + b));
           else
             ptx::mbar_arrive_cluster(bar0(L::bPFull + b));
         }
-        ++pv_cnt[b];  // PV(j) may be issued from here on
+        pv_par ^= 1u << b;  // PV(j) may be issued from here on
         const float pt = ex2(fmaf(tmax, c, -m_use));
         const float pt16 = unpack2<BF16>(pack2<BF16>(pt, 0.f)).x;
         l = alpha * l + sum;
@@ -561,6 +577,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
       // The epilogue must have read the previous unit's statistics.
       if (units_done > 0 && !wait_all(L::bStatsFree, (units_done - 1) & 1)) break;
       ++units_done;
+      if (quarter == 0) FATTN_TRACE_EV(k, kTraceUnit, 12);
       sRowL[r] = lr;
       sRowM[r] = (m + log2f(l)) * 0.69314718055994531f;  // natural-log LSE
       ptx::mbar_arrive(bar(L::bStats));
@@ -584,6 +601,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
       if (t >= p.total_units) continue;
       const PairUnit w = pair_unit<CAUSAL>(t, p);
       if (!wait_all(L::bStats, st_cnt & 1)) break;
+      if (quarter == 0) FATTN_TRACE_EV(k, kTraceUnit, 15);
       ++st_cnt;
       const float l = sRowL[r];
       const float lse = sRowM[r];
@@ -594,6 +612,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
       // publish the statistics while the last two P V MMAs still run) and
       // pass on the parity of an older phase.
       if (!wait_all(L::bODone, od_cnt & 1)) break;
+      if (quarter == 0) FATTN_TRACE_EV(k, kTraceUnit, 16);
       ++od_cnt;
       ptx::tc_fence_after();
       const float inv_l = 1.0f / l;
@@ -603,27 +622,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
       uint4* const orow = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.o) +
                                                    grow * (size_t)(D * 2));
       const uint32_t o_addr = tmem + lane_off + L::kColO;
-#pragma unroll 2
+      const bool o_aligned32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
+      // The next chunk's TMEM load is in flight while this one is scaled,
+      // packed and stored.
+      uint32_t u[32];
+      ptx::tmem_ld32(o_addr, u);
+#pragma unroll 4
       for (int ch = 0; ch < D / 32; ++ch) {
-        uint32_t u[32];
-        ptx::tmem_ld32(o_addr + ch * 32, u);
         ptx::tmem_wait_ld();
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           pk[e] = pack2<BF16>(__uint_as_float(u[2 * e]) * inv_l,
                               __uint_as_float(u[2 * e + 1]) * inv_l);
+        if (ch + 1 < D / 32) {
+          ptx::tmem_ld32(o_addr + (ch + 1) * 32, u);
+        } else {
+          // all of O is read: the next unit's first P V may overwrite it
+          // while the stores below run
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (quarter == 0) FATTN_TRACE_EV(k, kTraceUnit, 17);
+          if (lane == 0) ptx::mbar_arrive_cluster(bar0(L::bOEmpty));
+        }
         if (valid) {
+          // a thread writes its own 512-byte row: 32-byte stores when the
+          // output is 32-byte aligned, else 16-byte ones
+          if (o_aligned32) {
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            orow[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                           pk[4 * v4 + 3]);
+            for (int v8 = 0; v8 < 2; ++v8) {
+              uint32_t w8[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) w8[e] = pk[8 * v8 + e];
+              ptx::st_global_v8(orow + ch * 4 + 2 * v8, w8);
+            }
+          } else {
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              orow[ch * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                             pk[4 * v4 + 3]);
+          }
         }
       }
       if (valid) p.lse[grow] = lse;
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_cluster(bar0(L::bOEmpty));
     }
   }
 
