@@ -548,6 +548,8 @@ def run_fattn(args):
     outs = {c: (torch.empty_like(q), torch.empty((B, H, S), dtype=torch.float32, device=dev))
             for c in MASKS}
     stream = torch.cuda.Stream(dev)
+    # the launch stream does not wait for the default stream by itself
+    stream.wait_stream(torch.cuda.current_stream(dev))
     sptr = stream.cuda_stream
     code = fattn.FATTN_BF16 if w.dtype == "bf16" else fattn.FATTN_FP16
 
@@ -865,6 +867,7 @@ def run_per_config(torch, fattn, dev, stream, peaks, main_x=None, main_w=None):
         lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
         rows = (np.arange(w.B * w.H * w.S, dtype=np.int64) if w.B * w.H * w.S <= 4096
                 else head_rows(w.B, w.H, w.S, seed=w.seed + 7000))
+        stream.wait_stream(torch.cuda.current_stream(dev))  # the inputs' conversion
         for causal in w.causal:
             def launch():
                 rc = fattn.fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
@@ -949,6 +952,7 @@ def run_sweep(args):
         del x
         o = torch.empty_like(q)
         lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=dev)
+        stream.wait_stream(torch.cuda.current_stream(dev))  # the inputs' conversion
         for causal in w.causal:
             def launch():
                 rc = fattn.fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
@@ -1010,6 +1014,8 @@ def run_fp8(args):
     outs = {c: (torch.empty((B, H, S, D), dtype=torch.bfloat16, device=dev),
                 torch.empty((B, H, S), dtype=torch.float32, device=dev)) for c in MASKS}
     stream = torch.cuda.Stream(dev)
+    # the launch stream does not wait for the default stream by itself
+    stream.wait_stream(torch.cuda.current_stream(dev))
     sptr = stream.cuda_stream
     qs, ks, vs = x.descale
 
@@ -1276,6 +1282,8 @@ def run_kvcache(args, w):
     plan = fattn.fattn_kvcache_plan(B, H, Sq, Sk, D)
     ws = torch.empty(plan["workspace_bytes"], dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(dev)
+    # the launch stream does not wait for the default stream by itself
+    stream.wait_stream(torch.cuda.current_stream(dev))
     sptr = stream.cuda_stream
 
     def launch(qq, kk, vv, ll):

@@ -282,6 +282,20 @@ __device__ __forceinline__ void next_batch(const DecodeParams& p, Cursor& cur) {
   } while (cur.n_b == 0);
 }
 
+// Moves the cursor forward until pos (a tile index from cur.base) lies in
+// its batch.  False when the lengths read now put pos past the last batch:
+// that happens only when the lengths change while the call runs (the caller
+// writing them concurrently), and the kernels then stop instead of reading
+// outside their buffers.
+__device__ __forceinline__ bool seek(const DecodeParams& p, Cursor& cur, long long& pos) {
+  while (pos >= (long long)cur.n_b * p.H) {
+    if (cur.b >= p.B - 1) return false;
+    pos -= (long long)cur.n_b * p.H;
+    next_batch(p, cur);
+  }
+  return cur.b < p.B;
+}
+
 __device__ __forceinline__ long long range_start(long long g, long long T,
                                                  int n_warps) {
   return g * T / n_warps;
@@ -335,14 +349,12 @@ __global__ void __launch_bounds__(DecodeLayout<D, SQ>::kThreads, 1)
   long long lpos = t0 - lc.base;  // tile index inside batch lc.b
   long long cpos = lpos;
   auto issue = [&](int r) {       // load tile t0 + r into slot r & 1
-    while (lpos >= (long long)lc.n_b * p.H) {
-      lpos -= (long long)lc.n_b * p.H;
-      next_batch(p, lc);
-    }
-    const int h = (int)(lpos / lc.n_b);
-    const int kt = (int)(lpos % lc.n_b);
+    const bool found = seek(p, lc, lpos);
+    const int h = found ? (int)(lpos / lc.n_b) : 0;
+    const int kt = found ? (int)(lpos % lc.n_b) : 0;
     const int bh = lc.b * p.H + h;
-    if (lane == 0) {
+    if (lane == 0 && !found) ptx::mbar_arrive(bar0 + (r & 1) * 8);  // phase ends empty
+    if (lane == 0 && found) {
       const uint32_t slot = slot0 + (r & 1) * L::kSlotBytes;
       const uint32_t bar = bar0 + (r & 1) * 8;
       ptx::mbar_arrive_expect_tx(bar, L::kSlotBytes);
@@ -398,9 +410,11 @@ __global__ void __launch_bounds__(DecodeLayout<D, SQ>::kThreads, 1)
   int fail = 0;
   for (int r = 0; r < n_tiles; ++r) {
     // ---- which head and key tile
-    while (cpos >= (long long)cc.n_b * p.H) {
-      cpos -= (long long)cc.n_b * p.H;
-      next_batch(p, cc);
+    if (!seek(p, cc, cpos)) {
+      if (lane == 0) record_error(p.status, kErrInvalidArg, (kRoleLens << 8) | 1, blockIdx.x);
+      ok = false;
+      fail = r;
+      break;
     }
     const int h = (int)(cpos / cc.n_b);
     const int kt = (int)(cpos % cc.n_b);
@@ -419,7 +433,7 @@ __global__ void __launch_bounds__(DecodeLayout<D, SQ>::kThreads, 1)
       __syncwarp();
     }
     const int key0 = kt * kTileKeys;
-    const int nvalid = min(kTileKeys, cur_len - key0);
+    const int nvalid = max(0, min(kTileKeys, cur_len - key0));
 
     // ---- wait for the tile
     const uint32_t slot = slot0 + (r & 1) * L::kSlotBytes;

@@ -142,14 +142,12 @@ __global__ void __launch_bounds__(DecodeMmaLayout<D>::kThreads, 1)
   long long lpos = t0 - lc.base;
   long long cpos = lpos;
   auto issue = [&](int r) {  // load tile t0 + r into slot r & 1
-    while (lpos >= (long long)lc.n_b * p.H) {
-      lpos -= (long long)lc.n_b * p.H;
-      next_batch(p, lc);
-    }
-    const int h = (int)(lpos / lc.n_b);
-    const int kt = (int)(lpos % lc.n_b);
+    const bool found = seek(p, lc, lpos);
+    const int h = found ? (int)(lpos / lc.n_b) : 0;
+    const int kt = found ? (int)(lpos % lc.n_b) : 0;
     const int bh = lc.b * p.H + h;
-    if (lane == 0) {
+    if (lane == 0 && !found) ptx::mbar_arrive(bar0 + (r & 1) * 8);  // phase ends empty
+    if (lane == 0 && found) {
       const uint32_t slot = slot0 + (r & 1) * L::kSlotBytes;
       const uint32_t bar = bar0 + (r & 1) * 8;
       ptx::mbar_arrive_expect_tx(bar, L::kSlotBytes);
@@ -210,9 +208,11 @@ __global__ void __launch_bounds__(DecodeMmaLayout<D>::kThreads, 1)
   bool ok = true;
   int fail = 0;
   for (int r = 0; r < n_tiles; ++r) {
-    while (cpos >= (long long)cc.n_b * p.H) {
-      cpos -= (long long)cc.n_b * p.H;
-      next_batch(p, cc);
+    if (!seek(p, cc, cpos)) {
+      if (lane == 0) record_error(p.status, kErrInvalidArg, (kRoleLens << 8) | 1, blockIdx.x);
+      ok = false;
+      fail = r;
+      break;
     }
     const int h = (int)(cpos / cc.n_b);
     const int kt = (int)(cpos % cc.n_b);
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(DecodeMmaLayout<D>::kThreads, 1)
       }
     }
     const int key0 = kt * kTileKeys;
-    const int nvalid = min(kTileKeys, cur_len - key0);
+    const int nvalid = max(0, min(kTileKeys, cur_len - key0));
 
     const uint32_t slot = slot0 + (r & 1) * L::kSlotBytes;
     if (!ptx::mbar_wait_drain(bar0 + (r & 1) * 8, (r >> 1) & 1, p.timeout_ns)) {
