@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -63,11 +64,24 @@ const DriverFns& driver() {
   return fns;
 }
 
+// Counter pairs for the causal kernels' run-time unit assignment: each
+// launch takes the next pair (round robin) and its last CTA returns both
+// words to 0.  Launches that run at the same time (other streams or host
+// threads) get different pairs as long as fewer than kSchedSlots of them
+// are in flight at once.  Launches enqueued into a stream capture take their
+// pairs from a second ring of kSchedSlots: a captured launch keeps its pair
+// for every replay of the graph (replays of one graph never overlap), and
+// no ordinary launch can be handed the same pair.
+constexpr int kSchedSlots = 256;
+
 struct DeviceState {
   bool init = false;
   bool supported = false;
   int sms = 0;
   int* status = nullptr;  // kStatusWords ints, device memory
+  int* sched = nullptr;   // 2 * kSchedSlots pairs of ints, device memory, zeroed once
+  std::atomic<unsigned> sched_next{0};        // ordinary launches: pairs [0, kSchedSlots)
+  std::atomic<unsigned> sched_next_graph{0};  // captured launches: the next kSchedSlots
 };
 
 std::mutex g_mu;
@@ -125,10 +139,15 @@ int current_device(DeviceState** out, int* dev_out) {
     d.supported = (major == 10 && minor == 3);
     if (d.supported) {
       if (cudaMalloc(&d.status, sizeof(int) * kStatusWords) != cudaSuccess ||
-          cudaMemset(d.status, 0, sizeof(int) * kStatusWords) != cudaSuccess) {
+          cudaMemset(d.status, 0, sizeof(int) * kStatusWords) != cudaSuccess ||
+          cudaMalloc(&d.sched, sizeof(int) * 4 * kSchedSlots) != cudaSuccess ||
+          cudaMemset(d.sched, 0, sizeof(int) * 4 * kSchedSlots) != cudaSuccess ||
+          cudaDeviceSynchronize() != cudaSuccess) {
         cudaGetLastError();
         if (d.status) cudaFree(d.status);
+        if (d.sched) cudaFree(d.sched);
         d.status = nullptr;
+        d.sched = nullptr;
         return kErrCuda;
       }
     }
@@ -138,6 +157,33 @@ int current_device(DeviceState** out, int* dev_out) {
   *out = &d;
   if (dev_out) *dev_out = dev;
   return kOk;
+}
+
+// Heads per group of the causal order: as many as keep the group's K and V
+// (bytes_per_row per key row of one of them) within about a quarter of L2,
+// so the heads of the two groups in flight at a group change fit with room
+// for the query, output and other traffic.
+int causal_group_heads(int BH, int S, int bytes_per_row) {
+  const double per_head = 2.0 * (double)S * bytes_per_row;  // K and V of one head
+  int g = (int)(32.0 * 1024 * 1024 / per_head);
+  if (g < 1) g = 1;
+  return g > BH ? BH : g;
+}
+
+int* sched_pair(DeviceState* ds, cudaStream_t stream) {
+  // The legacy default stream is never captured itself (and querying it
+  // while another stream captures in global mode is an error), so only
+  // other streams are asked.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (stream != nullptr && cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    cs = cudaStreamCaptureStatusNone;
+  }
+  const bool captured = cs == cudaStreamCaptureStatusActive;
+  std::atomic<unsigned>& next = captured ? ds->sched_next_graph : ds->sched_next;
+  const unsigned slot = next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots +
+                        (captured ? kSchedSlots : 0);
+  return ds->sched + 2 * slot;
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -491,6 +537,12 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o,
   a.grid = fwd_grid(plan, D, causal != 0, bf16, ds->sms);
   if (a.grid <= 0) return FATTN_ERR_LAUNCH;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
+  // Causal kernels at D = 128 hand units out at run time over head groups
+  // and need a counter; D = 64 and D = 256 take static orders over every
+  // head.
+  const bool run_time_units = causal && D == 128;
+  a.params.sched = run_time_units ? sched_pair(ds, a.stream) : nullptr;
+  a.params.group_heads = run_time_units ? causal_group_heads(BH, S, D * 2) : BH;
 
   const cudaError_t e = D == 64    ? launch_fwd_d64(causal != 0, bf16, a)
                         : D == 128 ? launch_fwd_d128(causal != 0, bf16, a)
@@ -673,6 +725,8 @@ FATTN_API int fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   a.params.timeout_ns = wait_timeout_ns();
   a.grid = (int)total < ds->sms ? (int)total : ds->sms;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
+  a.params.sched = causal ? sched_pair(ds, a.stream) : nullptr;
+  a.params.group_heads = causal_group_heads(BH, S, D);
   if (launch_fwd_fp8_d128(causal != 0, out_dtype == FATTN_BF16, a) != cudaSuccess) {
     cudaGetLastError();
     return FATTN_ERR_LAUNCH;

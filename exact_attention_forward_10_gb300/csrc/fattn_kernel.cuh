@@ -97,6 +97,7 @@
 namespace fattn {
 
 constexpr int kTraceUnit = 71;
+constexpr int kUnitRing = 4;  // unit indices the load warp may publish ahead
 constexpr bool kSpinLoad = (FATTN_SPIN_ROLES & 1) != 0;
 constexpr bool kSpinMma = (FATTN_SPIN_ROLES & 2) != 0;
 constexpr bool kSpinSoftmax = (FATTN_SPIN_ROLES & 4) != 0;
@@ -121,6 +122,14 @@ struct FwdParams {
   float scale_log2;   // scale * log2(e) (FP8: times the Q and K scales)
   float o_scale;      // multiplies O in the epilogue (FP8: the V scale; else 1)
   unsigned long long timeout_ns;
+  // Causal masks: work units are handed out at run time from sched[0] (the
+  // next unit; sched[1] counts the CTAs done, and the last one resets both
+  // to 0), in groups of group_heads heads (longest units first within a
+  // group) so the K/V of the heads in flight stay in L2.  With sched null
+  // each CTA takes the units of its own slots of the snake order instead
+  // (group_heads then equal to BH: longest first over every head).
+  int* sched;
+  int group_heads;
 };
 
 // EB: bytes per input element (2: fp16/bf16; 1: E4M3).  A swizzle chunk is
@@ -150,11 +159,14 @@ struct FwdLayout {
   static constexpr int bDrain = bOEmpty + QT;
   static constexpr int bP1Full = bDrain + 1;         // first half of P_i ready
   static constexpr int bPV1Done = bP1Full + QT;      // its P V done
-  static constexpr int kNumBars = bPV1Done + QT;
+  static constexpr int bUnitFull = bPV1Done + QT;    // [kUnitRing] unit index published
+  static constexpr int bUnitEmpty = bUnitFull + kUnitRing;  // [kUnitRing] read by all
+  static constexpr int kNumBars = bUnitEmpty + kUnitRing;
   static constexpr int kMisc = kBars + kNumBars * 8;   // tmem base, abort flag
   static constexpr int kRowL = kMisc + 16;             // float [QT][128]
   static constexpr int kRowM = kRowL + QT * kBM * 4;   // float [QT][128]: LSE
-  static constexpr int kEnd = kRowM + QT * kBM * 4;
+  static constexpr int kUnitSlots = kRowM + QT * kBM * 4;  // int [kUnitRing]
+  static constexpr int kEnd = kUnitSlots + kUnitRing * 4;
   // The dynamic shared memory base must be 1024-byte aligned (128-byte
   // swizzle atoms); the kernel checks it instead of reserving slack.
   static constexpr int kSmemBytes = kEnd;
@@ -224,17 +236,25 @@ struct Unit {
 };
 
 // Work unit t -> (head, first query row, key-tile counts per query tile).
-// Causal units go longest first (the last query tiles need the most keys).
+// Causal units go longest first (the last query tiles need the most keys):
+// GROUPED, within groups of group_heads heads; else over every head.
 // Non-causal units of one head are adjacent, so CTAs running together share
 // that head's K/V in L2.
-template <int QT, bool CAUSAL>
+template <int QT, bool CAUSAL, bool GROUPED>
 __device__ __forceinline__ Unit decode_unit(int t, const FwdParams& p,
                                             int (&n)[QT]) {
   Unit w;
   int u;
-  if (CAUSAL) {
+  if (CAUSAL && !GROUPED) {
     u = p.n_units - 1 - t / p.BH;
     w.bh = t % p.BH;
+  } else if (CAUSAL) {
+    const int G = p.group_heads;
+    const int g = t / (G * p.n_units);
+    const int r = t - g * G * p.n_units;
+    const int gh = p.BH - g * G < G ? p.BH - g * G : G;
+    u = p.n_units - 1 - r / gh;
+    w.bh = g * G + r % gh;
   } else {
     u = t % p.n_units;
     w.bh = t / p.n_units;
@@ -348,15 +368,37 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                      const FwdParams p) {
   using L = FwdLayout<D, QT, NS, FP8 ? 1 : 2>;
   using W = FwdWarps<QT>;
+  // Causal units at D = 128 (16-bit and E4M3) are handed out at run time
+  // from the launch's counter (p.sched), in head groups; other kernels take
+  // a static snake over a fixed order.
+  constexpr bool kRunTimeUnits = CAUSAL && D == 128;
+  // warps that read the unit sequence: MMA issuers, softmax, epilogue
+  constexpr int kUnitReaders = 4 * QT + 4 + (L::kDualMma ? 2 : 1);
+  constexpr int kUnitEnd = -2;
   static_assert(!FP8 || !L::kSepP, "8-bit inputs use the layout where P overwrites S");
   extern __shared__ uint8_t smem_raw[];
 
+  // A run-time-unit kernel launched without its counter reports a launch
+  // error and does nothing (every CTA returns here).
+  if (kRunTimeUnits && p.sched == nullptr) {
+    if (threadIdx.x == 0 && atomicCAS(p.status, 0, kErrLaunch) == 0) {
+      p.status[1] = 0;
+      p.status[2] = (int)blockIdx.x;
+    }
+    return;
+  }
   const uint32_t base = ptx::smem_u32(smem_raw);
   if (base & 1023u) {
     // Not 1024-byte aligned: report instead of touching shared memory.
     if (threadIdx.x == 0 && atomicCAS(p.status, 0, kErrLaunch) == 0) {
       p.status[1] = 0;
       p.status[2] = (int)blockIdx.x;
+    }
+    // this CTA still counts as done, so the launch's unit counter is reset
+    if (kRunTimeUnits && threadIdx.x == 0 &&
+        atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(p.sched, 0);
+      atomicExch(p.sched + 1, 0);
     }
     return;
   }
@@ -394,6 +436,10 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       ptx::mbar_init(bar(L::bKVEmpty + s), 1);
     }
     ptx::mbar_init(bar(L::bDrain), L::kDualMma ? 2 : 1);
+    for (int r = 0; r < kUnitRing; ++r) {
+      ptx::mbar_init(bar(L::bUnitFull + r), 1);
+      ptx::mbar_init(bar(L::bUnitEmpty + r), kUnitReaders);
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -405,6 +451,32 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+
+  // The unit of this CTA's k-th round.  Run-time units (causal masks with a
+  // counter): the load warp takes units from the launch's counter and
+  // publishes them through a small ring (a value >= total_units ends the
+  // sequence).  Otherwise the static snake, where a round may have no unit
+  // for this CTA (a value >= total_units).  kUnitEnd ends the sequence; -1
+  // is an error.
+  int* const unit_slots = reinterpret_cast<int*>(smem + L::kUnitSlots);
+  auto next_unit = [&](int k, int role) -> int {
+    if constexpr (kRunTimeUnits) {
+      const int slot = k % kUnitRing;
+      bool w_ok = ptx::mbar_wait(bar(L::bUnitFull + slot), (k / kUnitRing) & 1, abort_flag, tmo);
+      w_ok = __all_sync(0xffffffffu, w_ok);
+      if (!w_ok) {
+        if (lane == 0) raise_error(p, abort_flag, kErrPipelineTimeout, role, L::bUnitFull + slot);
+        return -1;
+      }
+      const int t = *reinterpret_cast<volatile int*>(unit_slots + slot);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(L::bUnitEmpty + slot));
+      return t >= p.total_units ? kUnitEnd : t;
+    } else {
+      if (k * (int)gridDim.x >= p.total_units) return kUnitEnd;
+      return unit_of_round(k);
+    }
+  };
 
   // The register split is stated at the top of each role's branch so it
   // dominates that role's code.
@@ -423,11 +495,33 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       for (int i = 0; i < QT; ++i) q_uses[i] = 0;
       uint32_t kv_filled = 0, kv_fill_ph = 0;  // per stage: ever filled, parity
       bool ok = true;
-      for (int k = 0; ok && k * (int)gridDim.x < p.total_units; ++k) {
-        const int t = unit_of_round(k);
-        if (t >= p.total_units) continue;
+      // Run-time units: a CTA's first unit is its own index (the first
+      // gridDim.x units of the order), later ones come from the launch's
+      // counter.
+      int t_next = (int)blockIdx.x < p.total_units ? (int)blockIdx.x : p.total_units;
+      for (int k = 0; ok; ++k) {
+        int t;
+        if constexpr (kRunTimeUnits) {
+          // publish this unit to the other roles
+          t = t_next;
+          const int slot = k % kUnitRing;
+          if (k >= kUnitRing &&
+              !ptx::mbar_wait<kSpinLoad>(bar(L::bUnitEmpty + slot), ((k / kUnitRing) - 1) & 1,
+                                         abort_flag, tmo)) {
+            raise_error(p, abort_flag, kErrPipelineTimeout, kRoleLoad, L::bUnitEmpty + slot);
+            ok = false;
+            break;
+          }
+          *reinterpret_cast<volatile int*>(unit_slots + slot) = t;
+          ptx::mbar_arrive(bar(L::bUnitFull + slot));
+          if (t >= p.total_units) break;
+        } else {
+          if (k * (int)gridDim.x >= p.total_units) break;
+          t = unit_of_round(k);
+          if (t >= p.total_units) continue;
+        }
         int n[QT];
-        const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
+        const Unit w = decode_unit<QT, CAUSAL, kRunTimeUnits>(t, p, n);
         for (int i = 0; ok && i < QT; ++i) {
           if (n[i] == 0) continue;
           if (q_uses[i] > 0 &&
@@ -449,7 +543,13 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         // scores and P V issue apart, K_0, then K_{j+1} before V_j (the next
         // tile's scores are issued while this tile's softmax runs), so the
         // slots are released about in load order.
+        int taken = 0;  // causal: the counter's value for the next unit
         for (int it = 0; ok && it < 2 * w.n_max; ++it) {
+          // The next unit is taken as this unit's last key tile is loaded:
+          // the CTAs that will be free first take the longest units left;
+          // the atomic's result is first used after the loop, so its latency
+          // passes under the last copies.
+          if (kRunTimeUnits && it == 2 * w.n_max - 2) taken = atomicAdd(p.sched, 1);
           int j, kv;
           if constexpr (L::kDualMma) {
             if (it == 0) {
@@ -488,6 +588,10 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
               kv_ph ^= 1u;
             }
           }
+        }
+        if constexpr (kRunTimeUnits) {
+          t_next = (int)gridDim.x + taken;
+          if (t_next > p.total_units) t_next = p.total_units;
         }
       }
       // Never leave with copies in flight into this CTA's shared memory.
@@ -586,11 +690,16 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         }
       };
 
-      for (int k = 0; ok && k * (int)gridDim.x < p.total_units; ++k) {
-        const int t = unit_of_round(k);
+      for (int k = 0; ok; ++k) {
+        const int t = next_unit(k, kRoleMma);
+        if (t == kUnitEnd) break;
+        if (t < 0) {
+          ok = false;
+          break;
+        }
         if (t >= p.total_units) continue;
         int n[QT];
-        const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
+        const Unit w = decode_unit<QT, CAUSAL, kRunTimeUnits>(t, p, n);
         if (!L::kDualMma || s_role)
           for (int i = 0; ok && i < QT; ++i)
             if (n[i] > 0) {
@@ -900,11 +1009,12 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       const float2 s4 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
       return s4.x + s4.y;
     };
-    for (int k = 0; k * (int)gridDim.x < p.total_units; ++k) {
-      const int t = unit_of_round(k);
+    for (int k = 0;; ++k) {
+      const int t = next_unit(k, kRoleSoftmax);
+      if (t == kUnitEnd || t < 0) break;
       if (t >= p.total_units) continue;
       int n[QT];
-      const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
+      const Unit w = decode_unit<QT, CAUSAL, kRunTimeUnits>(t, p, n);
       const int nk = n[i];
       if (nk == 0) continue;
       // m: the row's reference maximum of scaled scores (log2 domain), moved
@@ -1200,11 +1310,16 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         raise_error(p, abort_flag, kErrPipelineTimeout, kRoleCorrection, slot);
       return w_ok;
     };
-    for (int k = 0; ok && k * (int)gridDim.x < p.total_units; ++k) {
-      const int t = unit_of_round(k);
+    for (int k = 0; ok; ++k) {
+      const int t = next_unit(k, kRoleCorrection);
+      if (t == kUnitEnd) break;
+      if (t < 0) {
+        ok = false;
+        break;
+      }
       if (t >= p.total_units) continue;
       int n[QT];
-      const Unit w = decode_unit<QT, CAUSAL>(t, p, n);
+      const Unit w = decode_unit<QT, CAUSAL, kRunTimeUnits>(t, p, n);
       // epilogue: O = acc / l (one reciprocal per row), LSE = ln2 (m + log2 l)
       for (int i = 0; i < QT; ++i) {
         if (n[i] == 0) continue;
@@ -1224,23 +1339,27 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
             reinterpret_cast<uint8_t*>(p.o) + grow * (size_t)(D * 2));
         const uint32_t o_addr = tmem + lane_off + L::colO(i);
         const bool o_aligned32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
+        // The next chunk's TMEM load is in flight while this one is scaled,
+        // packed and stored.
+        uint32_t u[32];
+        ptx::tmem_ld32(o_addr, u);
 #pragma unroll
         for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t u[32];
-          ptx::tmem_ld32(o_addr + ch * 32, u);
           ptx::tmem_wait_ld();
-          if (ch == D / 32 - 1) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            pk[e] = pack2<BF16>(__uint_as_float(u[2 * e]) * inv_l,
+                                __uint_as_float(u[2 * e + 1]) * inv_l);
+          if (ch + 1 < D / 32) {
+            ptx::tmem_ld32(o_addr + (ch + 1) * 32, u);
+          } else {
             // O_i (and the row statistics, read above) are in registers: the
             // next unit's P V may overwrite them while the stores below run.
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(L::bOEmpty + i));
             FATTN_TRACE_EV(k, kTraceUnit, 19 + i);
           }
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            pk[e] = pack2<BF16>(__uint_as_float(u[2 * e]) * inv_l,
-                                __uint_as_float(u[2 * e + 1]) * inv_l);
           if (valid) {
             // a thread writes its own row: 32-byte stores when the output is
             // 32-byte aligned (rows are 128 or 256 bytes), else 16-byte ones
@@ -1269,6 +1388,17 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
   if (warp == W::kMma) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+  if constexpr (CAUSAL) {
+    // Every unit this CTA will ever take has been taken; the last CTA to
+    // get here returns the launch's counter to 0 for the next launch.
+    if (kRunTimeUnits && threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+        atomicExch(p.sched, 0);
+        atomicExch(p.sched + 1, 0);
+      }
+    }
   }
 }
 

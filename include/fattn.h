@@ -19,8 +19,17 @@
  *
  * Ownership.  The caller owns and allocates every buffer (device memory).
  * The library allocates no user-visible memory; it keeps a small per-device
- * status block and per-kernel launch attributes for the life of the process.
- * Outputs may not overlap inputs or each other.
+ * status block, two rings of 256 work counters (4 KB) and per-kernel launch
+ * attributes for the life of the process.  Outputs may not overlap inputs or
+ * each other.
+ *
+ * Work counters.  A causal fattn_fwd / fattn_fwd_fp8 launch at D = 128 hands
+ * its work units out at run time from one counter pair, taken round robin
+ * from a ring of 256 per device; the launch's last CTA returns the pair to
+ * zero.  Up to 256 such launches may run at once on one device (more would
+ * share a pair).  A launch enqueued into a stream capture takes its pair from
+ * the second ring and keeps it for every replay of the graph; replays of one
+ * graph never overlap, and ordinary launches never use that ring.
  *
  * Asynchrony.  fattn_fwd enqueues the work on ``stream`` and returns; results
  * are visible after the stream is synchronised.
@@ -191,6 +200,11 @@ FATTN_API int fattn_plan(int B, int H, int S, int D, int causal, int *grid,
  *              is clamped for memory safety and reported by
  *              fattn_last_error as FATTN_ERR_INVALID_ARG (detail[0] = 6 << 8,
  *              detail[1] = the batch index); the outputs are then undefined.
+ *              The lengths must not change while the call runs (the kernels
+ *              read them several times); if they do, the kernels stop
+ *              without reading outside any buffer, report
+ *              FATTN_ERR_INVALID_ARG (detail[0] = 6 << 8 | 1) and leave the
+ *              outputs undefined.
  *   o          device [B, H, Sq, D] 16-bit output, 16-byte aligned
  *   lse        device [B, H, Sq] fp32 output, 4-byte aligned
  *   B, H       batch and heads (>= 1)

@@ -185,3 +185,47 @@ def test_output_alignment(D, offset_bytes):
                 f"D{D} offset {offset_bytes} causal={causal}")
         # the guard elements around O were not written
         assert torch.isnan(ob[:skip]).all() and torch.isnan(ob[skip + n:]).all()
+
+
+def test_causal_units_handed_out_at_run_time():
+    """Causal launches take their work units from a counter at run time
+    (each launch a counter of its own from a pool of 256, reset by the
+    launch's last CTA).  300 launches in a row, more than the pool, on two
+    shapes in turn: every output is bit-identical to the first (a unit's
+    result does not depend on which CTA computes it) and matches the
+    oracle."""
+    import math
+
+    import torch
+
+    import exact_attention_forward_10_gb300 as fattn
+    import oracle
+
+    dev = torch.device("cuda:0")
+    sets = []
+    for (B, H, S, D, seed) in ((2, 8, 1000, 64, 1401), (1, 12, 777, 128, 1402)):
+        x = attn_inputs.make_qkv(B, H, S, D, "fp16", seed=seed)
+        q, k, v = (torch.from_numpy(a).to(dev).to(torch.float16) for a in (x.q, x.k, x.v))
+        sets.append((x, q, k, v, B, H, S, D))
+    first = [None, None]
+    for it in range(300):
+        idx = it % 2
+        x, q, k, v, B, H, S, D = sets[idx]
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full((B, H, S), float("nan"), dtype=torch.float32, device=dev)
+        rc = fattn.fattn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                             B, H, S, D, True, 1.0 / math.sqrt(D), fattn.FATTN_FP16, 0)
+        assert rc == 0
+        if first[idx] is None:
+            torch.cuda.synchronize()
+            first[idx] = (o.clone(), lse.clone())
+        elif it % 37 == 0 or it >= 296:
+            torch.cuda.synchronize()
+            assert torch.equal(o, first[idx][0]) and torch.equal(lse, first[idx][1]), it
+    torch.cuda.synchronize()
+    assert fattn.fattn_last_error(0)[0] == 0
+    for idx in range(2):
+        x, q, k, v, B, H, S, D = sets[idx]
+        ro, rl = oracle.attn_fwd(x.q, x.k, x.v, True, 1.0 / math.sqrt(D))
+        compare(first[idx][0].double().cpu().numpy(), first[idx][1].double().cpu().numpy(),
+                ro, rl, "fp16", f"run-time units {B}x{H}x{S}x{D}")
