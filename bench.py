@@ -125,13 +125,33 @@ def gather_rows(torch, o, lse, rows):
             lse.reshape(-1).index_select(0, idx).double().cpu().numpy())
 
 
-def workload_config(w, extra=None) -> dict:
+# GB300's L2 (126.5 MiB), rounded up.  A timed launch whose inputs are
+# smaller than this runs after an L2 flush (a write of twice its size
+# outside the launch's own CUDA events).
+L2_BYTES = 129 * 2**20
+
+
+def l2_flush_buffer(torch, dev, input_bytes: int):
+    """The buffer to overwrite before each timed launch, or None when the
+    launch's inputs are larger than L2."""
+    if input_bytes > L2_BYTES:
+        return None
+    return torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+
+
+def l2_label(input_bytes: int, what: str = "Q,K,V") -> str:
+    if input_bytes > L2_BYTES:
+        return f"inputs larger than L2 ({what} {input_bytes / 2**20:.0f} MiB); no flush"
+    return (f"inputs smaller than L2 ({what} {input_bytes / 2**20:.0f} MiB): L2 flushed "
+            f"(a {2 * L2_BYTES / 2**20:.0f} MiB write) before each timed launch, outside its "
+            "CUDA events; the step time is the sum of the launches' event times")
+
+
+def workload_config(w, extra=None, elem_bytes: int = 2) -> dict:
     c = {"workload": f"B{w.B} H{w.H} S{w.S} D{w.D} {w.dtype}, non-causal + "
                      f"causal, Q/K/V iid N(0,1) seed {w.seed}, scale 1/sqrt(D)",
          "B": w.B, "H": w.H, "S": w.S, "D": w.D, "masks": "non-causal+causal",
-         "l2": (f"inputs larger than L2 (Q,K,V {3 * 2 * w.B * w.H * w.S * w.D / 2**20:.0f} MiB); "
-                "no flush") if 3 * 2 * w.B * w.H * w.S * w.D > 160e6 else
-               "inputs smaller than L2; no flush between steps"}
+         "l2": l2_label(3 * elem_bytes * w.B * w.H * w.S * w.D)}
     if extra:
         c.update(extra)
     return c
@@ -578,6 +598,7 @@ def run_fattn(args):
     n_ev = args.steps * len(MASKS)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n_ev)]
+    flush = l2_flush_buffer(torch, dev, 3 * 2 * B * H * S * D)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             for c in MASKS:
@@ -593,6 +614,8 @@ def run_fattn(args):
         e = 0
         for _ in range(args.steps):
             for c in MASKS:
+                if flush is not None:
+                    flush.add_(1)
                 ev[e][0].record(stream)
                 launch(c, q, k, v)
                 ev[e][1].record(stream)
@@ -604,6 +627,8 @@ def run_fattn(args):
     per_launch = {c: [] for c in MASKS}
     for i, (a, b) in enumerate(ev):
         per_launch[MASKS[i % len(MASKS)]].append(a.elapsed_time(b))
+    if flush is not None:  # the flushes are not part of the step
+        elapsed_ms = sum(a.elapsed_time(b) for a, b in ev)
     rc, where = fattn.fattn_last_error(sptr)
     if rc != 0:
         raise RuntimeError(f"kernel status {rc} at {where}")
@@ -929,7 +954,8 @@ def run_sweep(args):
     with ``--csv PATH`` the same points as CSV.
     Each point runs on its seeded input set (seed 4 + index, the sets the
     parity tests compare with the oracle); generating them on the host takes
-    most of the sweep's wall time."""
+    most of the sweep's wall time.  Points whose inputs are smaller than L2
+    are timed after an L2 flush outside each launch's events."""
     import torch
 
     import exact_attention_forward_10_gb300 as fattn
@@ -964,15 +990,19 @@ def run_sweep(args):
                 for _ in range(args.warmup):
                     launch()
             torch.cuda.synchronize(dev)
+            flush = l2_flush_buffer(torch, dev, 3 * 2 * w.B * w.H * w.S * w.D)
             times = []
             for _ in range(max(20, args.steps)):
                 a = torch.cuda.Event(enable_timing=True)
                 b = torch.cuda.Event(enable_timing=True)
                 with torch.cuda.stream(stream):
+                    if flush is not None:
+                        flush.add_(1)
                     a.record(stream)
                     launch()
                     b.record(stream)
                 times.append((a, b))
+            del flush
             torch.cuda.synchronize(dev)
             ms = statistics.median(x.elapsed_time(y) for x, y in times)
             rc, where = fattn.fattn_last_error(stream.cuda_stream)
@@ -1045,6 +1075,7 @@ def run_fp8(args):
     barrier()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps * len(MASKS))]
+    flush = l2_flush_buffer(torch, dev, 3 * B * H * S * D)  # one-byte inputs
     sampler = clock_sampler(dev)
     sampler.start()
     time.sleep(0.05)
@@ -1055,6 +1086,8 @@ def run_fp8(args):
         e = 0
         for _ in range(args.steps):
             for c in MASKS:
+                if flush is not None:
+                    flush.add_(1)
                 ev[e][0].record(stream)
                 launch(c, q, k, v)
                 ev[e][1].record(stream)
@@ -1069,6 +1102,8 @@ def run_fp8(args):
     for i, (a, b) in enumerate(ev):
         per_launch[MASKS[i % len(MASKS)]].append(a.elapsed_time(b))
     step_ms = t0.elapsed_time(t1) / args.steps
+    if flush is not None:  # the flushes are not part of the step
+        step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
 
     h_outs = {c: (torch.empty((B, H, S, D), dtype=torch.bfloat16).pin_memory(),
                   torch.empty((B, H, S), dtype=torch.float32).pin_memory()) for c in MASKS}
@@ -1125,7 +1160,8 @@ def run_fp8(args):
             "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
             "config": workload_config(w, {"inputs": "E4M3 codes, per-tensor power-of-two "
                                                     "scales", "output": "bf16",
-                                          "parallelism": f"replicas x{world}"}),
+                                          "parallelism": f"replicas x{world}"},
+                                      elem_bytes=1),
             "per_mask": per_mask,
             # E4M3 Q, K, V (1 byte each) read once, bf16 O and fp32 LSE written once
             "hbm_gbs": world * len(MASKS) * B * H * S * (5 * D + 4) / (step_ms * 1e-3) / 1e9,
@@ -1168,13 +1204,13 @@ def kv_bytes(w, lens) -> int:
             + w.B * w.H * w.Sq * 4)
 
 
-def kv_config(w, extra=None) -> dict:
+def kv_config(w, cached_lens, extra=None) -> dict:
     lens = (f"cached lengths uniform in [{w.lens_range[0]}, {w.lens_range[1]}] "
             f"(seed {w.seed})" if w.lens_range else f"every length {w.Sk}")
     c = {"workload": f"{w.name}: Q/K/V iid N(0,1) seed {w.seed}, {lens}, "
                      f"{'causal' if w.causal else 'non-causal'}, scale 1/sqrt(D)",
          "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk, "D": w.D,
-         "l2": "cache larger than L2; no flush"}
+         "l2": l2_label(kv_bytes(w, cached_lens), "bytes read per call")}
     if extra:
         c.update(extra)
     return c
@@ -1239,7 +1275,7 @@ def run_kvcache_reference(args, w):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * tot_t / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": kv_config(w, {"parallelism": "host cores, rank 0 only"}),
+        "config": kv_config(w, x.lens, {"parallelism": "host cores, rank 0 only"}),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -1311,6 +1347,7 @@ def run_kvcache(args, w):
     barrier()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
+    flush = l2_flush_buffer(torch, dev, kv_bytes(w, x.lens))
     sampler = clock_sampler(dev)
     sampler.start()
     time.sleep(0.05)
@@ -1319,6 +1356,8 @@ def run_kvcache(args, w):
     with torch.cuda.stream(stream):
         t0.record(stream)
         for a, b in ev:
+            if flush is not None:
+                flush.add_(1)
             a.record(stream)
             launch(q, k, v, lens)
             b.record(stream)
@@ -1330,6 +1369,8 @@ def run_kvcache(args, w):
         raise RuntimeError(f"kernel status {rc} at {where}")
     step_ms = t0.elapsed_time(t1) / args.steps
     call_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if flush is not None:  # the flushes are not part of the step
+        step_ms = call_ms
 
     # end to end: the caches are the sequences' state, resident on the GPU
     # across steps (as in decoding, where each step's new keys and values are
@@ -1381,7 +1422,7 @@ def run_kvcache(args, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
-            "config": kv_config(w, {"parallelism": f"replicas x{world}",
+            "config": kv_config(w, x.lens, {"parallelism": f"replicas x{world}",
                                     "grid": plan["grid"], "block": plan["block"],
                                     "split_warps": plan["split_warps"],
                                     "bytes_per_call": byts}),

@@ -537,10 +537,10 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o,
   a.grid = fwd_grid(plan, D, causal != 0, bf16, ds->sms);
   if (a.grid <= 0) return FATTN_ERR_LAUNCH;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
-  // Causal kernels at D = 128 hand units out at run time over head groups
-  // and need a counter; D = 64 and D = 256 take static orders over every
+  // Causal kernels at D = 128 and 256 hand units out at run time over head
+  // groups and need a counter; D = 64 takes the static order over every
   // head.
-  const bool run_time_units = causal && D == 128;
+  const bool run_time_units = causal && (D == 128 || D == 256);
   a.params.sched = run_time_units ? sched_pair(ds, a.stream) : nullptr;
   a.params.group_heads = run_time_units ? causal_group_heads(BH, S, D * 2) : BH;
 

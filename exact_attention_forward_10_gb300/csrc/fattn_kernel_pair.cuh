@@ -81,11 +81,14 @@ struct PairLayout {
   static constexpr int bStats = bOEmpty + 1;      // each CTA: 128 arrivals
   static constexpr int bStatsFree = bStats + 1;   // each CTA: 4 warp arrivals
   static constexpr int bDrain = bStatsFree + 1;   // rank 0: MMA drain
-  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int bUnitFull = bDrain + 1;    // [kUnitRing] each CTA: rank 0's load warp
+  static constexpr int bUnitEmpty = bUnitFull + kUnitRing;  // [kUnitRing] rank 0: every reader
+  static constexpr int kNumBars = bUnitEmpty + kUnitRing;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kRowL = kMisc + 16;
   static constexpr int kRowM = kRowL + kBM * 4;
-  static constexpr int kSmemBytes = kRowM + kBM * 4;
+  static constexpr int kUnitSlots = kRowM + kBM * 4;  // int [kUnitRing]
+  static constexpr int kSmemBytes = kUnitSlots + kUnitRing * 4;
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   __host__ __device__ static constexpr uint32_t colS(int b) { return 128u * b; }
   static constexpr uint32_t kColO = 128u * NSB;
@@ -114,14 +117,19 @@ struct PairUnit {
 };
 
 // Unit t: causal units longest first (the last query blocks need the most
-// keys); non-causal units of one head adjacent (they share its K/V in L2).
+// keys) within groups of group_heads heads, so the K/V of the heads in flight
+// stay in L2; non-causal units of one head adjacent (they share its K/V).
 template <bool CAUSAL>
 __device__ __forceinline__ PairUnit pair_unit(int t, const FwdParams& p) {
   PairUnit w;
   int u;
   if (CAUSAL) {
-    u = p.n_units - 1 - t / p.BH;
-    w.bh = t % p.BH;
+    const int G = p.group_heads;
+    const int g = t / (G * p.n_units);
+    const int r = t - g * G * p.n_units;
+    const int gh = p.BH - g * G < G ? p.BH - g * G : G;
+    u = p.n_units - 1 - r / gh;
+    w.bh = g * G + r % gh;
   } else {
     u = t % p.n_units;
     w.bh = t / p.n_units;
@@ -155,8 +163,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
   constexpr int kQBytes = L::kQBytes;
   constexpr int kItemBytes = L::kItemBytes;
   using W = PairWarps;
+  // every warp that reads the unit sequence, in both CTAs: softmax (4) and
+  // epilogue (4) in each, rank 0's MMA warp and rank 1's load warp
+  constexpr int kUnitReaders = 18;
+  constexpr int kUnitEnd = -2;
   extern __shared__ uint8_t smem_raw[];
 
+  // A causal launch without its unit counter reports a launch error and
+  // does nothing (every CTA of every cluster returns here).
+  if (CAUSAL && p.sched == nullptr) {
+    if (threadIdx.x == 0 && atomicCAS(p.status, 0, kErrLaunch) == 0) {
+      p.status[1] = 0;
+      p.status[2] = (int)blockIdx.x;
+    }
+    return;
+  }
   const uint32_t base = ptx::smem_u32(smem_raw);
   // Both CTAs of a cluster get the same layout; a misaligned base would be
   // the same in both, so both return here and neither waits for the other.
@@ -164,6 +185,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
     if (threadIdx.x == 0 && atomicCAS(p.status, 0, kErrLaunch) == 0) {
       p.status[1] = 0;
       p.status[2] = (int)blockIdx.x;
+    }
+    // this CTA still counts as done, so the launch's unit counter is reset
+    if (CAUSAL && threadIdx.x == 0 && atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+      atomicExch(p.sched, 0);
+      atomicExch(p.sched + 1, 0);
     }
     return;
   }
@@ -202,6 +228,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
     ptx::mbar_init(bar(L::bStats), kBM);
     ptx::mbar_init(bar(L::bStatsFree), 4);
     ptx::mbar_init(bar(L::bDrain), 1);
+    for (int r = 0; r < kUnitRing; ++r) {
+      ptx::mbar_init(bar(L::bUnitFull + r), 1);
+      ptx::mbar_init(bar(L::bUnitEmpty + r), kUnitReaders);
+    }
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -223,7 +253,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
     }
     *abort_flag = 1;
   };
-  const int rounds = (p.total_units + (int)gridDim.x / 2 - 1) / ((int)gridDim.x / 2);
+  // The unit of this CTA pair's k-th round.  Causal: rank 0's load warp
+  // takes units at run time (its cluster's index first, then the launch's
+  // counter) and writes each into a small ring in both CTAs; every reader
+  // hands its slot back to rank 0.  A value >= total_units ends the
+  // sequence.  Non-causal: the static snake, where a round may have no unit
+  // for this pair (a value >= total_units).  kUnitEnd ends the sequence; -1
+  // is an error.
+  const int n_clusters = (int)gridDim.x / 2;
+  volatile int* const unit_slots = reinterpret_cast<volatile int*>(smem + L::kUnitSlots);
+  // one lane's read of unit k (the load warp of rank 1 runs in one lane)
+  auto read_unit = [&](int k, int role) -> int {
+    const int slot = k % kUnitRing;
+    if (!ptx::mbar_wait_cluster(bar(L::bUnitFull + slot), (k / kUnitRing) & 1, abort_flag, tmo)) {
+      fail(role, L::bUnitFull + slot);
+      return -1;
+    }
+    const int t = unit_slots[slot];
+    ptx::mbar_arrive_cluster(bar0(L::bUnitEmpty + slot));
+    return t >= p.total_units ? kUnitEnd : t;
+  };
+  auto next_unit = [&](int k, int role) -> int {
+    if constexpr (CAUSAL) {
+      const int slot = k % kUnitRing;
+      bool w_ok = ptx::mbar_wait_cluster(bar(L::bUnitFull + slot), (k / kUnitRing) & 1,
+                                         abort_flag, tmo);
+      w_ok = __all_sync(0xffffffffu, w_ok);
+      if (!w_ok) {
+        if (lane == 0) fail(role, L::bUnitFull + slot);
+        return -1;
+      }
+      const int t = unit_slots[slot];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(bar0(L::bUnitEmpty + slot));
+      return t >= p.total_units ? kUnitEnd : t;
+    } else {
+      if (k * n_clusters >= p.total_units) return kUnitEnd;
+      return pair_unit_of_round(k);
+    }
+  };
 
   if (warp >= W::kMma) ptx::setmaxnreg_dec<W::kRegOther>();
 
@@ -237,10 +305,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
       int q_uses = 0;
       uint32_t filled = 0, fill_ph = 0;
       bool ok = true;
-      for (int k = 0; ok && k < rounds; ++k) {
-        const int t = pair_unit_of_round(k);
-        if (t >= p.total_units) continue;
+      int t_next = (int)blockIdx.x / 2 < p.total_units ? (int)blockIdx.x / 2 : p.total_units;
+      for (int k = 0; ok; ++k) {
+        int t;
+        if constexpr (CAUSAL) {
+          if (leader) {
+            // publish unit k in both CTAs' rings
+            t = t_next;
+            const int slot = k % kUnitRing;
+            if (k >= kUnitRing &&
+                !ptx::mbar_wait_cluster(bar(L::bUnitEmpty + slot), ((k / kUnitRing) - 1) & 1,
+                                        abort_flag, tmo)) {
+              fail(kRoleLoad, L::bUnitEmpty + slot);
+              ok = false;
+              break;
+            }
+            unit_slots[slot] = t;
+            ptx::st_shared_cluster_u32(ptx::mapa_shared(base + L::kUnitSlots + 4u * slot, 1),
+                                       (uint32_t)t);
+            ptx::mbar_arrive(bar(L::bUnitFull + slot));
+            ptx::mbar_arrive_cluster(ptx::mapa_shared(bar(L::bUnitFull + slot), 1));
+            if (t >= p.total_units) break;
+          } else {
+            t = read_unit(k, kRoleLoad);
+            if (t == kUnitEnd) break;
+            if (t < 0) {
+              ok = false;
+              break;
+            }
+          }
+        } else {
+          if (k * n_clusters >= p.total_units) break;
+          t = pair_unit_of_round(k);
+          if (t >= p.total_units) continue;
+        }
         const PairUnit w = pair_unit<CAUSAL>(t, p);
+        int taken = 0;  // causal, rank 0: the counter's value for the next unit
         if (q_uses > 0 &&
             !ptx::mbar_wait_cluster(bar(L::bQEmpty), (q_uses - 1) & 1, abort_flag, tmo)) {
           fail(kRoleLoad, L::bQEmpty);
@@ -255,6 +355,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
                                 c * kSwizzleChunkCols, w.row0 + kBM * (int)rank, w.bh);
         ++q_uses;
         for (int j = 0; ok && j < w.n; ++j) {
+          // The next unit is taken as this unit's last key tile is loaded:
+          // the pairs that will be free first take the longest units left.
+          if (CAUSAL && leader && j == w.n - 1) taken = atomicAdd(p.sched, 1);
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
             if (!ptx::mbar_wait_cluster(bar(L::bKVEmpty + idx), ph ^ 1u, abort_flag, tmo)) {
@@ -286,6 +389,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
               idx = 0;
               ph ^= 1u;
             }
+          }
+        }
+        if constexpr (CAUSAL) {
+          if (leader) {
+            t_next = n_clusters + taken;
+            if (t_next > p.total_units) t_next = p.total_units;
           }
         }
       }
@@ -355,8 +464,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
             ptx::mma_ts_pair<1>(d, a + kk * 8, vb + kk * (2048 >> 4), kHi, kIdPV, 1u);
         }
       };
-      for (int k = 0; ok && k < rounds; ++k) {
-        const int t = pair_unit_of_round(k);
+      for (int k = 0; ok; ++k) {
+        const int t = next_unit(k, kRoleMma);
+        if (t == kUnitEnd) break;
+        if (t < 0) {
+          ok = false;
+          break;
+        }
         if (t >= p.total_units) continue;
         const PairUnit w = pair_unit<CAUSAL>(t, p);
         const uint32_t ubase = item;
@@ -470,8 +584,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
       const float2 s4 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
       return s4.x + s4.y;
     };
-    for (int k = 0; ok && k < rounds; ++k) {
-      const int t = pair_unit_of_round(k);
+    for (int k = 0; ok; ++k) {
+      const int t = next_unit(k, kRoleSoftmax);
+      if (t == kUnitEnd) break;
+      if (t < 0) {
+        ok = false;
+        break;
+      }
       if (t >= p.total_units) continue;
       const PairUnit w = pair_unit<CAUSAL>(t, p);
       const int row = w.row0 + kBM * (int)rank + r;  // this thread's query row
@@ -596,8 +715,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
       if (!w_ok && lane == 0) fail(kRoleCorrection, slot);
       return w_ok;
     };
-    for (int k = 0; ok && k < rounds; ++k) {
-      const int t = pair_unit_of_round(k);
+    for (int k = 0; ok; ++k) {
+      const int t = next_unit(k, kRoleCorrection);
+      if (t == kUnitEnd) break;
+      if (t < 0) {
+        ok = false;
+        break;
+      }
       if (t >= p.total_units) continue;
       const PairUnit w = pair_unit<CAUSAL>(t, p);
       if (!wait_all(L::bStats, st_cnt & 1)) break;
@@ -676,6 +800,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairWarps::kThreads,
   if (warp == W::kMma) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc_pair(tmem, kTmemCols);
+  }
+  if constexpr (CAUSAL) {
+    // Every unit this pair will take has been taken; the last CTA to get
+    // here returns the launch's counter to 0 for the next launch.
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+        atomicExch(p.sched, 0);
+        atomicExch(p.sched + 1, 0);
+      }
+    }
   }
 }
 

@@ -435,6 +435,12 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
+// Store a 32-bit word at a shared::cluster address (it may be in the peer
+// CTA); a later release-arrive orders it for the reader.
+__device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
 // Arrive on a barrier given by its shared::cluster address (it may live in
 // the peer CTA), with release semantics at cluster scope.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {

@@ -211,3 +211,17 @@ def test_per_config_workloads_are_the_named_sets():
     for dt in ("fp16", "bf16"):
         w = got[f"5 S8192 D64 {dt}"]
         assert (w.S, w.D, w.dtype) == (8192, 64, dt) and w.causal == (False, True)
+
+
+def test_l2_policy_flushes_working_sets_under_l2():
+    """Timed launches whose inputs fit in L2 are preceded by a flush; the
+    label says which, and the benchmark workload's inputs are larger."""
+    small = bench.l2_label(96 * 2**20)
+    big = bench.l2_label(192 * 2**20)
+    assert "flushed" in small and "smaller than L2" in small
+    assert "larger than L2" in big and "no flush" in big
+    # the cache workload of B8 H16 Sq4 D64 reads ~126 MB a call: under L2
+    w = attn_inputs.CACHE_WORKLOADS["decode_b8_h16_sq4_d64"]
+    lens = attn_inputs.cache_lengths(w.seed, w.B, *w.lens_range)
+    assert bench.kv_bytes(w, lens) < bench.L2_BYTES
+    assert "flushed" in bench.kv_config(w, lens)["l2"]
