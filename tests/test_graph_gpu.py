@@ -117,12 +117,17 @@ def test_graph_replay_equals_eager_call(torch, label, kind, causal):
     assert np.isfinite(lse.cpu().numpy()).all(), label
 
 
-def test_graph_of_cache_attention(torch):
+@pytest.mark.parametrize("Sq,D", [(4, 128), (1, 64), (1, 128)])
+def test_graph_of_cache_attention(torch, Sq, D):
+    """Cache attention captured and replayed, one and several new queries,
+    with a batch that has no cached key: every replay equals the eager
+    call."""
     import exact_attention_forward_10_gb300 as fattn
 
     dev = torch.device("cuda:0")
-    x = attn_inputs.make_kvcache(4, 8, 4, 3000, 128, "bf16", seed=9300,
+    x = attn_inputs.make_kvcache(4, 8, Sq, 3000, D, "bf16", seed=9300 + Sq + D,
                                  lens_range=(1, 3000))
+    x.lens[1] = 0
     tdt = torch_dtype("bf16")
     q, kc, vc = (torch.from_numpy(a).to(dev).to(tdt) for a in (x.q, x.k, x.v))
     lens = torch.as_tensor(x.lens, dtype=torch.int32, device=dev)
