@@ -753,6 +753,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                 ptx::tc_fence_after();
                 FATTN_TRACE_EV(k, j, 26 + 2 * i);
                 issue_s(i, (uint32_t)item_slot(k_item(j)));
+                FATTN_TRACE_EV(k, j, 13 + i);
                 commit(L::bSFull + i);
                 if (j == n[i] - 1) commit(L::bQEmpty + i);
                 if (i == last_user(j)) commit(L::bKVEmpty + item_slot(k_item(j)));
@@ -780,6 +781,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                 FATTN_TRACE_EV(k, j, 25 + 2 * i);
                 ptx::tc_fence_after();
                 issue_pv(i, (uint32_t)item_slot(v_item(j)), j > 0);
+                FATTN_TRACE_EV(k, j, 15 + i);
                 commit(L::bPVDone + i);
                 if (i == last_user(j)) commit(L::bKVEmpty + item_slot(v_item(j)));
               }

@@ -239,3 +239,17 @@ def test_causal_units_handed_out_at_run_time():
         ro, rl = oracle.attn_fwd(x.q, x.k, x.v, True, 1.0 / math.sqrt(D), rows=rows)
         compare(o.reshape(-1, D)[rows], lse.reshape(-1)[rows], ro, rl, "fp16",
                 f"run-time units {B}x{H}x{S}x{D}")
+
+
+@pytest.mark.parametrize("B,H,S,D,dtype", [
+    (3, 12, 4096, 128, "bf16"),   # 36 heads in groups of 16, 16 and 4
+    (1, 20, 4096, 256, "fp16"),   # 20 heads in groups of 8, 8 and 4
+    (1, 7, 4097, 256, "bf16"),    # ragged S, one partial group
+])
+def test_causal_head_groups_with_remainder(B, H, S, D, dtype):
+    """Causal units in L2-sized head groups whose last group is smaller than
+    the others, and a ragged sequence: sampled rows of every head against
+    the oracle."""
+    x = attn_inputs.make_qkv(B, H, S, D, dtype, seed=1600 + H + D)
+    check_sampled(x, True, seed=1600 + H, label=f"B{B} H{H} S{S} D{D} {dtype} causal",
+                  stride=128)
