@@ -244,7 +244,7 @@ def test_causal_units_handed_out_at_run_time():
 @pytest.mark.parametrize("B,H,S,D,dtype", [
     (3, 12, 4096, 128, "bf16"),   # 36 heads in groups of 16, 16 and 4
     (1, 20, 4096, 256, "fp16"),   # 20 heads in groups of 8, 8 and 4
-    (1, 7, 4097, 256, "bf16"),    # ragged S, one partial group
+    (1, 11, 4097, 256, "bf16"),   # ragged S: 11 heads in groups of 7 and 4
 ])
 def test_causal_head_groups_with_remainder(B, H, S, D, dtype):
     """Causal units in L2-sized head groups whose last group is smaller than
