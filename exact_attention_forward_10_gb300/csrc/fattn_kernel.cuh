@@ -87,6 +87,23 @@
 #define FATTN_D64_SCORE_PER_TILE 0
 #endif
 
+// 16-bit inputs, shared score buffer: a row's later key tiles exponentiate
+// against the reference chosen after the tile before, taking the tile's
+// maximum in the same pass; a tile whose maximum passed that reference by
+// more than kRescaleLog2 moves it for the next tile (its own P, in the old
+// frame, stays below 2^kOverflowLog2), and only a tile whose 16-bit P could
+// overflow is redone.  Otherwise each tile takes its maximum first.  Bits:
+// 0 head dim 64, 1 head dim 128 non-causal, 2 head dim 128 causal, 3 fp16
+// inputs too (else bf16 only).  A build-time choice; the default, bf16 head
+// dim 128 non-causal, is where it measured faster (B2 H16 S8192 bf16 at
+// 2070 MHz: 1797-1813 TF against 1611-1639 on N(0,1) inputs; 1521-1538
+// against 1703-1711 with Q, K x 4; causal 1420-1477 against 1543-1553; head
+// dim 64 945-1020 against 1050-1124; fp16 with Q, K x 4, where 2^15 bounds
+// the lag, 1267-1274 against 1687-1690).
+#ifndef FATTN_FUSED_MAX
+#define FATTN_FUSED_MAX 2
+#endif
+
 // Roles whose barrier waits spin instead of suspending (bit 0: load warp,
 // bit 1: MMA warp, bit 2: softmax warps waiting for scores); a build-time
 // choice.
@@ -109,6 +126,13 @@ constexpr uint32_t kTmemCols = 512;
 // A row's reference maximum moves only when the new maximum exceeds it by
 // more than this (log2 units), so every p = exp2(s*c - m) stays <= 2^8.
 constexpr float kRescaleLog2 = 8.0f;
+// With the maximum taken during the exponent pass (FATTN_FUSED_MAX) a tile's
+// P is computed against the previous tile's reference; it is redone only
+// when a weight could pass 2^kOverflowLog2: 2^15 < 65504 for fp16 P; bf16
+// P, whose range is that of fp32, is redone past 2^64 (O and l, fp32, stay
+// far from overflow: 128 keys x 2^64 x |v|).
+template <bool BF16>
+constexpr float kOverflowLog2 = BF16 ? 64.0f : 15.0f;
 
 struct FwdParams {
   void* o;            // [BH, S, D] 16-bit
@@ -372,6 +396,9 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
   // from the launch's counter (p.sched), in head groups; other kernels take
   // a static snake over a fixed order.
   constexpr bool kRunTimeUnits = CAUSAL && D == 128;
+  constexpr bool kFusedMax =
+      !FP8 && (L::kSepP || L::kShareS) && (BF16 || (FATTN_FUSED_MAX & 8) != 0) &&
+      (FATTN_FUSED_MAX & (D == 64 ? 1 : D != 128 ? 0 : CAUSAL ? 4 : 2)) != 0;
   // warps that read the unit sequence: MMA issuers, softmax, epilogue
   constexpr int kUnitReaders = 4 * QT + 4 + (L::kDualMma ? 2 : 1);
   constexpr int kUnitEnd = -2;
@@ -925,11 +952,11 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       const float2 c2 = make_float2(c, c);
       const float2 neg2 = make_float2(-mref, -mref);
       float2 sum2[4];
-      float acc[8];
+      float acc[4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) sum2[a] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int a = 0; a < 8; ++a) acc[a] = -INFINITY;
+      for (int a = 0; a < 4; ++a) acc[a] = -INFINITY;
       [[maybe_unused]] float r0 = 0.f, r1 = 0.f;
 #pragma unroll
       for (int ch = 0; ch < kN / 32; ++ch) {
@@ -938,7 +965,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const float s0 = s[kFirst + ch * 32 + 2 * e], s1 = s[kFirst + ch * 32 + 2 * e + 1];
-          if (kTrack) acc[e & 7] = fmax3(acc[e & 7], s0, s1);
+          if (kTrack) acc[e & 3] = fmax3(acc[e & 3], s0, s1);
           const float2 x = __ffma2_rn(make_float2(s0, s1), c2, neg2);
           const float2 pp = make_float2(ex2(x.x), ex2(x.y));
           sum2[e & 3] = __fadd2_rn(sum2[e & 3], pp);
@@ -961,9 +988,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           ptx::tmem_st16(addr + ch * 16, pk);
         }
       }
-      if (kTrack)
-        tmax = fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
-                     fmaxf(acc[6], acc[7]));
+      if (kTrack) tmax = fmaxf(fmax3(acc[0], acc[1], acc[2]), acc[3]);
       if constexpr (FP8) rsum = r0 + r1;
       const float2 s4 = __fadd2_rn(__fadd2_rn(sum2[0], sum2[1]), __fadd2_rn(sum2[2], sum2[3]));
       return s4.x + s4.y;
@@ -1023,6 +1048,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       // only when a new maximum exceeds it by more than kRescaleLog2; l: the
       // running sum of exp2(s*c - m) with that same reference.
       float m = -INFINITY;
+      float m_next = 0.f;  // fused maximum: the reference for the next tile
       float l = 0.f;   // sum of fp32 p (log-sum-exp)
       float lr = 0.f;  // the same with each tile's largest p rounded as the
                        // MMA multiplies it (normaliser of O)
@@ -1066,16 +1092,60 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           for (int e = 0; e < kBN; ++e) s[e] = e < limit ? s[e] : -INFINITY;
         }
         float m_use = m, alpha = 1.0f, sum, tmax, rsum = 0.f;
-        if constexpr (L::kSepP || L::kShareS) {
+        if constexpr (kFusedMax) {
+          // Maximum fused into the exponent pass.  The first tile of a row
+          // takes its maximum first; a later one uses the reference chosen
+          // after the tile before (m_next), so its weights may pass 2^8 (by
+          // as much as that tile's maximum passed the reference) and the
+          // reference, when it moves, moves one tile late: O and l stay in
+          // one frame with each tile's P.  Only a tile whose weights could
+          // overflow the 16-bit P is redone, against its own maximum.
+          if (j == 0) {
+            float acc[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) acc[a] = fmax3(s[2 * a], s[2 * a + 1], -INFINITY);
+#pragma unroll
+            for (int e = 16; e < kBN; e += 16) {
+#pragma unroll
+              for (int a = 0; a < 8; ++a) acc[a] = fmax3(acc[a], s[e + 2 * a], s[e + 2 * a + 1]);
+            }
+            m_use = c * fmax3(fmax3(acc[0], acc[1], acc[2]), fmax3(acc[3], acc[4], acc[5]),
+                              fmaxf(acc[6], acc[7]));
+            if (m_use == -INFINITY) m_use = 0.f;  // no allowed key in this row
+          } else {
+            m_use = m_next;
+          }
+          FATTN_TRACE_EV(k, j, 8 * i + 3);
+          // P_i's columns are free, and O_i complete through tile j-1, once
+          // the P V that read the previous P has landed.
+          if (p_writes > 0) {
+            bool w_ok = ptx::mbar_wait(bar(L::bPVDone + i), (p_writes - 1) & 1, abort_flag, tmo);
+            w_ok = __all_sync(0xffffffffu, w_ok);
+            if (!w_ok) {
+              if (lane == 0) raise_error(p, abort_flag, kErrPipelineTimeout, kRoleSoftmax, L::bPVDone + i);
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+          }
+          ++p_writes;
+          sum = exp_pass(s, m_use, p_addr, std::true_type{}, tmax, rsum, KeyRange<0, kBN>{});
+          {
+            const bool ovf = tmax * c > m_use + kOverflowLog2<BF16>;
+            if (__any_sync(0xffffffffu, ovf)) {
+              if (ovf) m_use = tmax * c;
+              sum = exp_pass(s, m_use, p_addr, std::false_type{}, tmax, rsum, KeyRange<0, kBN>{});
+            }
+          }
+          if (j > 0 && m_use != m) alpha = ex2(m - m_use);
+          m_next = tmax * c > m_use + kRescaleLog2 ? tmax * c : m_use;
+        } else if constexpr (L::kSepP || L::kShareS) {
           // Separate P, maximum first: the exponents go to registers at once
           // and P to TMEM once the previous P V has landed (no redo is
-          // possible once packed P waits in registers for its buffer).
-          // Waiting for that P V first and exponentiating against the
-          // current reference with the maximum on the side (as P over S
-          // does) saves the maximum pass, but measured slower on scores that
-          // spread widely (Q, K x 4: 1190 against 1617-1667 TF at B2 H16
-          // S8192 D128, a redo in nearly every tile) and for causal masks,
-          // and within 1-9% faster only at head dim 128 on N(0,1) inputs.
+          // possible once packed P waits in registers for its buffer).  The
+          // fused form above saves the maximum pass but waits for that P V
+          // before its exponents; it measured faster only for bf16
+          // non-causal at head dim 128 (FATTN_FUSED_MAX).
           float acc[8];
 #pragma unroll
           for (int a = 0; a < 8; ++a) acc[a] = fmax3(s[2 * a], s[2 * a + 1], -INFINITY);
