@@ -392,10 +392,12 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
                      const FwdParams p) {
   using L = FwdLayout<D, QT, NS, FP8 ? 1 : 2>;
   using W = FwdWarps<QT>;
-  // Causal units at D = 128 (16-bit and E4M3) are handed out at run time
-  // from the launch's counter (p.sched), in head groups; other kernels take
-  // a static snake over a fixed order.
-  constexpr bool kRunTimeUnits = CAUSAL && D == 128;
+  // Causal units at D = 128 (16-bit and E4M3) may be handed out at run time
+  // from the launch's counter (p.sched, set by the host when the K and V of
+  // all heads exceed what L2 keeps), in head groups; otherwise, and in the
+  // other kernels, each CTA takes a static snake over a fixed order.
+  constexpr bool kRunTimeCapable = CAUSAL && D == 128;
+  const bool run_time_units = kRunTimeCapable && p.sched != nullptr;
   constexpr bool kFusedMax =
       !FP8 && (L::kSepP || L::kShareS) && (BF16 || (FATTN_FUSED_MAX & 8) != 0) &&
       (FATTN_FUSED_MAX & (D == 64 ? 1 : D != 128 ? 0 : CAUSAL ? 4 : 2)) != 0;
@@ -405,15 +407,6 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
   static_assert(!FP8 || !L::kSepP, "8-bit inputs use the layout where P overwrites S");
   extern __shared__ uint8_t smem_raw[];
 
-  // A run-time-unit kernel launched without its counter reports a launch
-  // error and does nothing (every CTA returns here).
-  if (kRunTimeUnits && p.sched == nullptr) {
-    if (threadIdx.x == 0 && atomicCAS(p.status, 0, kErrLaunch) == 0) {
-      p.status[1] = 0;
-      p.status[2] = (int)blockIdx.x;
-    }
-    return;
-  }
   const uint32_t base = ptx::smem_u32(smem_raw);
   if (base & 1023u) {
     // Not 1024-byte aligned: report instead of touching shared memory.
@@ -422,7 +415,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       p.status[2] = (int)blockIdx.x;
     }
     // this CTA still counts as done, so the launch's unit counter is reset
-    if (kRunTimeUnits && threadIdx.x == 0 &&
+    if (run_time_units && threadIdx.x == 0 &&
         atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
       atomicExch(p.sched, 0);
       atomicExch(p.sched + 1, 0);
@@ -487,7 +480,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
   // is an error.
   int* const unit_slots = reinterpret_cast<int*>(smem + L::kUnitSlots);
   auto next_unit = [&](int k, int role) -> int {
-    if constexpr (kRunTimeUnits) {
+    if (run_time_units) {
       const int slot = k % kUnitRing;
       bool w_ok = ptx::mbar_wait(bar(L::bUnitFull + slot), (k / kUnitRing) & 1, abort_flag, tmo);
       w_ok = __all_sync(0xffffffffu, w_ok);
@@ -528,7 +521,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       int t_next = (int)blockIdx.x < p.total_units ? (int)blockIdx.x : p.total_units;
       for (int k = 0; ok; ++k) {
         int t;
-        if constexpr (kRunTimeUnits) {
+        if (run_time_units) {
           // publish this unit to the other roles
           t = t_next;
           const int slot = k % kUnitRing;
@@ -548,7 +541,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           if (t >= p.total_units) continue;
         }
         int n[QT];
-        const Unit w = decode_unit<QT, CAUSAL, kRunTimeUnits>(t, p, n);
+        const Unit w = decode_unit<QT, CAUSAL, kRunTimeCapable>(t, p, n);
         for (int i = 0; ok && i < QT; ++i) {
           if (n[i] == 0) continue;
           if (q_uses[i] > 0 &&
@@ -576,7 +569,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
           // the CTAs that will be free first take the longest units left;
           // the atomic's result is first used after the loop, so its latency
           // passes under the last copies.
-          if (kRunTimeUnits && it == 2 * w.n_max - 2) taken = atomicAdd(p.sched, 1);
+          if (run_time_units && it == 2 * w.n_max - 2) taken = atomicAdd(p.sched, 1);
           int j, kv;
           if constexpr (L::kDualMma) {
             if (it == 0) {
@@ -616,7 +609,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
             }
           }
         }
-        if constexpr (kRunTimeUnits) {
+        if (run_time_units) {
           t_next = (int)gridDim.x + taken;
           if (t_next > p.total_units) t_next = p.total_units;
         }
@@ -726,7 +719,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
         }
         if (t >= p.total_units) continue;
         int n[QT];
-        const Unit w = decode_unit<QT, CAUSAL, kRunTimeUnits>(t, p, n);
+        const Unit w = decode_unit<QT, CAUSAL, kRunTimeCapable>(t, p, n);
         if (!L::kDualMma || s_role)
           for (int i = 0; ok && i < QT; ++i)
             if (n[i] > 0) {
@@ -1041,7 +1034,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       if (t == kUnitEnd || t < 0) break;
       if (t >= p.total_units) continue;
       int n[QT];
-      const Unit w = decode_unit<QT, CAUSAL, kRunTimeUnits>(t, p, n);
+      const Unit w = decode_unit<QT, CAUSAL, kRunTimeCapable>(t, p, n);
       const int nk = n[i];
       if (nk == 0) continue;
       // m: the row's reference maximum of scaled scores (log2 domain), moved
@@ -1391,7 +1384,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
       }
       if (t >= p.total_units) continue;
       int n[QT];
-      const Unit w = decode_unit<QT, CAUSAL, kRunTimeUnits>(t, p, n);
+      const Unit w = decode_unit<QT, CAUSAL, kRunTimeCapable>(t, p, n);
       // epilogue: O = acc / l (one reciprocal per row), LSE = ln2 (m + log2 l)
       for (int i = 0; i < QT; ++i) {
         if (n[i] == 0) continue;
@@ -1464,7 +1457,7 @@ __global__ void __launch_bounds__(FwdWarps<QT>::kThreads, 1)
   if constexpr (CAUSAL) {
     // Every unit this CTA will ever take has been taken; the last CTA to
     // get here returns the launch's counter to 0 for the next launch.
-    if (kRunTimeUnits && threadIdx.x == 0) {
+    if (run_time_units && threadIdx.x == 0) {
       __threadfence();
       if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
         atomicExch(p.sched, 0);

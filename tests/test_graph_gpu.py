@@ -6,8 +6,10 @@ at 0), and a replay after the inputs are overwritten in place computes on
 the new values.  Captured launches take their counters from a ring of their
 own, so ordinary launches made between replays stay correct too.
 
-Every case has more work units than the GPU has SMs, so the causal cases
-hand units out at run time on every replay."""
+Every case has more work units than the GPU has SMs.  The causal cases at
+D = 256, at D = 128 with S = 4096 and in E4M3 with S = 8192 (K and V of all
+heads over 32 MiB) hand units out at run time on every replay; the D = 128
+case with S = 2048 takes the static order."""
 from __future__ import annotations
 
 import math
@@ -35,8 +37,9 @@ def torch():
 
 def _device_inputs(torch, kind, seed):
     dev = torch.device("cuda:0")
-    if kind == "fp8":
-        x = attn_inputs.make_qkv_fp8(2, 16, 2048, 128, seed=seed)
+    if isinstance(kind, str) and kind.startswith("fp8"):
+        S = int(kind[3:] or 2048)
+        x = attn_inputs.make_qkv_fp8(2, 16, S, 128, seed=seed)
         return x, [torch.from_numpy(a).to(dev) for a in (x.q8, x.k8, x.v8)]
     B, H, S, D, dtype = kind
     x = attn_inputs.make_qkv(B, H, S, D, dtype, seed=seed)
@@ -46,7 +49,7 @@ def _device_inputs(torch, kind, seed):
 
 def _call(fattn, kind, x, inp, causal, o, lse):
     q, k, v = inp
-    if kind == "fp8":
+    if isinstance(kind, str) and kind.startswith("fp8"):
         fattn.forward_fp8(q, k, v, *x.descale, causal=causal, out_dtype=o.dtype,
                           out=o, lse=lse)
     else:
@@ -54,11 +57,13 @@ def _call(fattn, kind, x, inp, causal, o, lse):
 
 
 CASES = [
-    ("D128 bf16 causal", (2, 16, 2048, 128, "bf16"), True),
+    ("D128 bf16 causal", (2, 16, 4096, 128, "bf16"), True),
+    ("D128 fp16 causal static", (2, 16, 2048, 128, "fp16"), True),
     ("D128 fp16", (2, 16, 2048, 128, "fp16"), False),
     ("D64 fp16 causal", (2, 16, 2048, 64, "fp16"), True),
     ("D256 bf16 causal", (2, 16, 2048, 256, "bf16"), True),
     ("E4M3 D128 causal", "fp8", True),
+    ("E4M3 D128 causal S8192", "fp88192", True),
 ]
 
 
@@ -68,7 +73,7 @@ def test_graph_replay_equals_eager_call(torch, label, kind, causal):
 
     x, inp = _device_inputs(torch, kind, seed=9100)
     shape = inp[0].shape
-    odt = torch.bfloat16 if kind == "fp8" else inp[0].dtype
+    odt = torch.bfloat16 if isinstance(kind, str) else inp[0].dtype
     B, H, S, _ = shape
 
     def outputs():

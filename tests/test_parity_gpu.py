@@ -189,9 +189,10 @@ def test_output_alignment(D, offset_bytes):
 
 
 def test_causal_units_handed_out_at_run_time():
-    """Causal launches at D = 128 and 256 take their work units from a
-    counter at run time (each launch a counter of its own from a pool of
-    256, reset by the launch's last CTA), in head groups sized to L2.  The
+    """Causal launches at D = 256, and at D = 128 when the K and V of all
+    heads exceed 32 MiB (64 MiB here), take their work units from a counter
+    at run time (each launch a counter of its own from a pool of 256, reset
+    by the launch's last CTA), in head groups sized to L2.  The
     shapes have several times more units than CTAs (pairs) and several head
     groups, so most units are fetched from the counter.  300 launches in a
     row, more than the pool, on the shapes in turn: every output is
