@@ -160,14 +160,30 @@ int current_device(DeviceState** out, int* dev_out) {
 }
 
 // Heads per group of the causal order: as many as keep the group's K and V
+// (bytes_per_row per key row of one of them) within group_mib MiB of L2, so
+// that the heads of the groups in flight at a group change fit with room for
+// the query, output and other traffic.
+// Heads per group of the causal order: as many as keep the group's K and V
 // (bytes_per_row per key row of one of them) within about a quarter of L2,
-// so the heads of the two groups in flight at a group change fit with room
-// for the query, output and other traffic.
-int causal_group_heads(int BH, int S, int bytes_per_row) {
+// so that the heads of the two groups in flight at a group change fit with
+// room for the query, output and other traffic.  The groups are made
+// near-equal: each group restarts the longest-first order, so a small last
+// group hands its longest units out last, when most CTAs are nearly done.
+// With min_units > 0 (units of a group, n_units per head), groups are also
+// merged while one would hold fewer than min_units units, since a group
+// change is a restart of the order that only enough units after it can even
+// out.  Measured at D = 128 (B2 H16 S4097 bf16 causal, K and V just over
+// 64 MiB): groups of 15, 15 and 2 heads 944 TF, 11, 11 and 10 1117-1120,
+// 16 and 16 1219-1222; B3 H11 S4096 in 16, 16 and 1 heads 917-921, in 11, 11
+// and 11 1082, in 17 and 16 1189-1214.
+int causal_group_heads(int BH, int S, int bytes_per_row, int n_units, int min_units) {
   const double per_head = 2.0 * (double)S * bytes_per_row;  // K and V of one head
   int g = (int)(32.0 * 1024 * 1024 / per_head);
   if (g < 1) g = 1;
-  return g > BH ? BH : g;
+  if (g >= BH) return BH;
+  int groups = (BH + g - 1) / g;
+  while (groups > 1 && (long long)((BH + groups - 1) / groups) * n_units < min_units) --groups;
+  return (BH + groups - 1) / groups;
 }
 
 int* sched_pair(DeviceState* ds, cudaStream_t stream) {
@@ -539,12 +555,16 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o,
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   // Causal kernels at D = 256 hand units out at run time over head groups
   // and need a counter; so do those at D = 128 when the K and V of all heads
-  // exceed one group (what L2 keeps).  Otherwise (and at D = 64) each CTA
-  // takes the static snake over the longest-first order of every head: with
-  // K and V resident in L2 the order costs no DRAM traffic, and the static
-  // order measured faster (B1 H32 S2048 D128 fp16 causal: 975-989 against
-  // 886-892 TF).
-  const int group = causal ? causal_group_heads(BH, S, D * 2) : BH;
+  // exceed one group.  Otherwise (and at D = 64) each CTA takes the static
+  // snake over the longest-first order of every head: with K and V resident
+  // in L2 the order costs no DRAM traffic, and the static order measured
+  // faster (B1 H32 S2048 D128 fp16 causal: 926-934 against 879 TF).  At
+  // D = 128 groups hold at least 1.5 units per CTA; on the CTA pairs merging
+  // measured no gain (B2 H16 S4097 D256: 1041 against 1110 TF in two groups
+  // of 16 rather than 32 MiB ones).
+  const int group = causal ? causal_group_heads(BH, S, D * 2, plan.units_per_head,
+                                                D == 128 ? 3 * ds->sms / 2 : 0)
+                           : BH;
   const bool run_time_units = causal && (D == 256 || (D == 128 && group < BH));
   a.params.sched = run_time_units ? sched_pair(ds, a.stream) : nullptr;
   a.params.group_heads = run_time_units ? group : BH;
@@ -732,7 +752,7 @@ FATTN_API int fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   // as for 16-bit inputs at D = 128: units at run time only when the K and
   // V of all heads exceed one group
-  const int group = causal ? causal_group_heads(BH, S, D) : BH;
+  const int group = causal ? causal_group_heads(BH, S, D, units_per_head, 3 * ds->sms / 2) : BH;
   a.params.sched = causal && group < BH ? sched_pair(ds, a.stream) : nullptr;
   a.params.group_heads = a.params.sched != nullptr ? group : BH;
   if (launch_fwd_fp8_d128(causal != 0, out_dtype == FATTN_BF16, a) != cudaSuccess) {

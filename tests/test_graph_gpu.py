@@ -7,9 +7,10 @@ the new values.  Captured launches take their counters from a ring of their
 own, so ordinary launches made between replays stay correct too.
 
 Every case has more work units than the GPU has SMs.  The causal cases at
-D = 256, at D = 128 with S = 4096 and in E4M3 with S = 8192 (K and V of all
-heads over 32 MiB) hand units out at run time on every replay; the D = 128
-case with S = 2048 takes the static order."""
+D = 256, at D = 128 with H = 20, S = 4096 and in E4M3 with S = 16384 (K and
+V of all heads over 32 MiB) hand units out at run time on every replay; the
+D = 128 case with S = 2048 and the E4M3 one with S = 2048 take the static
+order."""
 from __future__ import annotations
 
 import math
@@ -57,13 +58,13 @@ def _call(fattn, kind, x, inp, causal, o, lse):
 
 
 CASES = [
-    ("D128 bf16 causal", (2, 16, 4096, 128, "bf16"), True),
+    ("D128 bf16 causal", (2, 20, 4096, 128, "bf16"), True),
     ("D128 fp16 causal static", (2, 16, 2048, 128, "fp16"), True),
     ("D128 fp16", (2, 16, 2048, 128, "fp16"), False),
     ("D64 fp16 causal", (2, 16, 2048, 64, "fp16"), True),
     ("D256 bf16 causal", (2, 16, 2048, 256, "bf16"), True),
     ("E4M3 D128 causal", "fp8", True),
-    ("E4M3 D128 causal S8192", "fp88192", True),
+    ("E4M3 D128 causal S16384", "fp816384", True),
 ]
 
 

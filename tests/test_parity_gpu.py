@@ -190,7 +190,7 @@ def test_output_alignment(D, offset_bytes):
 
 def test_causal_units_handed_out_at_run_time():
     """Causal launches at D = 256, and at D = 128 when the K and V of all
-    heads exceed 32 MiB (64 MiB here), take their work units from a counter
+    heads exceed 64 MiB (96 MiB here), take their work units from a counter
     at run time (each launch a counter of its own from a pool of 256, reset
     by the launch's last CTA), in head groups sized to L2.  The
     shapes have several times more units than CTAs (pairs) and several head
@@ -207,9 +207,9 @@ def test_causal_units_handed_out_at_run_time():
 
     dev = torch.device("cuda:0")
     sets = []
-    # D128: 64 heads x 8 units (two groups of 32 heads); D256: 40 heads x 8
-    # pair units (groups of 16, 16 and 8 heads)
-    for (B, H, S, D, seed) in ((1, 64, 2048, 128, 1401), (1, 40, 2048, 256, 1402)):
+    # D128: 96 heads x 8 units (three groups of 32 heads); D256: 40 heads x 8
+    # pair units (three groups of 14, 14 and 12 heads)
+    for (B, H, S, D, seed) in ((1, 96, 2048, 128, 1401), (1, 40, 2048, 256, 1402)):
         x = attn_inputs.make_qkv(B, H, S, D, "fp16", seed=seed)
         q, k, v = (torch.from_numpy(a).to(dev).to(torch.float16) for a in (x.q, x.k, x.v))
         sets.append((x, q, k, v, B, H, S, D))
@@ -243,9 +243,9 @@ def test_causal_units_handed_out_at_run_time():
 
 
 @pytest.mark.parametrize("B,H,S,D,dtype", [
-    (3, 12, 4096, 128, "bf16"),   # 36 heads in groups of 16, 16 and 4
-    (1, 20, 4096, 256, "fp16"),   # 20 heads in groups of 8, 8 and 4
-    (1, 11, 4097, 256, "bf16"),   # ragged S: 11 heads in groups of 7 and 4
+    (3, 11, 4096, 128, "bf16"),   # 33 heads in groups of 17 and 16
+    (1, 20, 4096, 256, "fp16"),   # 20 heads in groups of 7, 7 and 6
+    (1, 11, 4097, 256, "bf16"),   # ragged S: 11 heads in groups of 6 and 5
 ])
 def test_causal_head_groups_with_remainder(B, H, S, D, dtype):
     """Causal units in L2-sized head groups whose last group is smaller than
