@@ -259,6 +259,35 @@ struct Unit {
   int n_max;
 };
 
+// Causal order over head groups: ng = ceil(BH / G) groups, the first
+// BH - ng (G - 1) of them of G heads and the rest of G - 1 (the host passes
+// G = ceil(BH / groups), so no group is more than one head smaller than
+// another; a small last group would hand its longest units out last).
+// Unit t of the order -> its rank within its head (longest first) and head.
+struct GroupPos {
+  int rank;
+  int bh;
+};
+__device__ __forceinline__ GroupPos group_position(int t, int BH, int G, int nu) {
+  const int ng = (BH + G - 1) / G;
+  const int big = BH - ng * (G - 1);      // groups of G heads (all of them when G == 1)
+  const int big_units = big * G * nu;
+  GroupPos gp;
+  if (t < big_units) {
+    const int g = t / (G * nu);
+    const int r = t - g * G * nu;
+    gp.rank = r / G;
+    gp.bh = g * G + r % G;
+  } else {
+    const int t2 = t - big_units;         // here G >= 2
+    const int g = t2 / ((G - 1) * nu);
+    const int r = t2 - g * (G - 1) * nu;
+    gp.rank = r / (G - 1);
+    gp.bh = big * G + g * (G - 1) + r % (G - 1);
+  }
+  return gp;
+}
+
 // Work unit t -> (head, first query row, key-tile counts per query tile).
 // Causal units go longest first (the last query tiles need the most keys):
 // GROUPED, within groups of group_heads heads; else over every head.
@@ -273,12 +302,9 @@ __device__ __forceinline__ Unit decode_unit(int t, const FwdParams& p,
     u = p.n_units - 1 - t / p.BH;
     w.bh = t % p.BH;
   } else if (CAUSAL) {
-    const int G = p.group_heads;
-    const int g = t / (G * p.n_units);
-    const int r = t - g * G * p.n_units;
-    const int gh = p.BH - g * G < G ? p.BH - g * G : G;
-    u = p.n_units - 1 - r / gh;
-    w.bh = g * G + r % gh;
+    const GroupPos gp = group_position(t, p.BH, p.group_heads, p.n_units);
+    u = p.n_units - 1 - gp.rank;
+    w.bh = gp.bh;
   } else {
     u = t % p.n_units;
     w.bh = t / p.n_units;
