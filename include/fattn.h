@@ -25,7 +25,9 @@
  *
  * Work counters.  A causal fattn_fwd launch at D = 256, and a causal
  * fattn_fwd_fp8 launch or a causal fattn_fwd launch at D = 128 whose K and V
- * (all heads) exceed 32 MiB, hands its work units out at run time from one
+ * (all heads) exceed 32 MiB and split into more than one head group (each
+ * group holding at least 1.5 work units per SM), hands its work units out
+ * at run time from one
  * counter pair, taken round robin from a ring of 256 per device; the
  * launch's last CTA returns the pair to zero.  Up to 256 such launches may
  * run at once on one device (more would share a pair).  A launch enqueued into a stream capture takes its pair from
