@@ -65,6 +65,17 @@ def test_stress_large_scores(dtype):
         check_full(x, causal, f"x4 {dtype} causal={causal}")
 
 
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_tile_maxima_jumping_past_the_overflow_cap(dtype):
+    """Q, K x 8: score std ~64 (~92 log2 units), so a key tile's maximum
+    often passes the reference chosen after the tile before by more than
+    2^64 (the bf16 non-causal kernel's redo of a tile) and nearly every
+    tile moves the reference."""
+    x = attn_inputs.make_qkv(2, 3, 1000, 128, dtype, seed=19, qk_mult=8.0)
+    for causal in (False, True):
+        check_full(x, causal, f"x8 {dtype} causal={causal}")
+
+
 def test_config_tiny():
     w = attn_inputs.WORKLOADS["tiny"]
     check_full(w.inputs(), False, w.name)
