@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
         l.fattn_error_string.restype = ctypes.c_char_p
         l.fattn_plan.argtypes = [i, i, i, i, i, ip, ip, ip, ip, ip, ip]
         l.fattn_plan.restype = i
+        l.fattn_causal_order.argtypes = [i, i, i, i, i, i, ip, ip]
+        l.fattn_causal_order.restype = i
         l.fattn_check_wait_timeout.argtypes = [i, vp]
         l.fattn_check_wait_timeout.restype = i
         u64 = ctypes.c_ulonglong
@@ -119,6 +121,17 @@ def fattn_plan(B, H, S, D, causal=False) -> dict:
     keys = ("grid", "block", "smem_bytes", "units", "q_tiles_per_unit",
             "kv_stages")
     return {k_: x.value for k_, x in zip(keys, vals)}
+
+
+def fattn_causal_order(B, H, S, D, elem_bytes=2, sms=152) -> dict:
+    """The work order of a causal launch (heads per group, units handed out
+    at run time or not) on a device with ``sms`` SMs; host only."""
+    g, rt = ctypes.c_int(), ctypes.c_int()
+    rc = lib().fattn_causal_order(B, H, S, D, elem_bytes, sms, ctypes.byref(g),
+                                  ctypes.byref(rt))
+    if rc != FATTN_OK:
+        raise FattnError(rc, "fattn_causal_order")
+    return {"group_heads": g.value, "run_time": bool(rt.value)}
 
 
 def fattn_fwd_fp8(q, k, v, o, lse, B, H, S, D, causal, scale, q_scale, k_scale,

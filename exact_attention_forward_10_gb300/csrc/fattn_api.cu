@@ -186,6 +186,20 @@ int causal_group_heads(int BH, int S, int bytes_per_row, int n_units, int min_un
   return (BH + groups - 1) / groups;
 }
 
+// The causal order of a launch: heads per group and whether units are handed
+// out at run time.  The CTA pairs (D = 256) always take them at run time, in
+// 32 MiB groups; D = 128 (16-bit, or E4M3 with elem_bytes 1) only when the
+// heads form more than one group, each holding at least 1.5 units per SM;
+// otherwise, and at D = 64, every head is in one group and each CTA takes
+// the static snake.
+void causal_order(int BH, int S, int D, int elem_bytes, int units_per_head, int sms,
+                  int* group_heads, bool* run_time) {
+  const int g = causal_group_heads(BH, S, D * elem_bytes, units_per_head,
+                                   D == 128 ? 3 * sms / 2 : 0);
+  *run_time = D == 256 || (D == 128 && g < BH);
+  *group_heads = *run_time ? g : BH;
+}
+
 int* sched_pair(DeviceState* ds, cudaStream_t stream) {
   // The legacy default stream is never captured itself (and querying it
   // while another stream captures in global mode is an error), so only
@@ -492,6 +506,21 @@ FATTN_API int fattn_plan(int B, int H, int S, int D, int causal, int* grid,
   return kOk;
 }
 
+FATTN_API int fattn_causal_order(int B, int H, int S, int D, int elem_bytes, int sms,
+                                 int* group_heads, int* run_time) {
+  if (sms < 1 || (elem_bytes != 1 && elem_bytes != 2)) return kErrInvalidArg;
+  if (elem_bytes == 1 && D != 128) return kErrUnsupported;
+  Plan plan;
+  const int rc = host_checks(B, H, S, D, &plan);
+  if (rc != kOk) return rc;
+  int g = B * H;
+  bool rt = false;
+  causal_order(B * H, S, D, elem_bytes, plan.units_per_head, sms, &g, &rt);
+  if (group_heads) *group_heads = g;
+  if (run_time) *run_time = rt ? 1 : 0;
+  return kOk;
+}
+
 FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o,
                         float* lse, int B, int H, int S, int D, int causal,
                         float scale, int dtype, fattn_stream_t stream) {
@@ -562,12 +591,11 @@ FATTN_API int fattn_fwd(const void* q, const void* k, const void* v, void* o,
   // D = 128 groups hold at least 1.5 units per CTA; on the CTA pairs merging
   // measured no gain (B2 H16 S4097 D256: 1041 against 1110 TF in two groups
   // of 16 rather than 32 MiB ones).
-  const int group = causal ? causal_group_heads(BH, S, D * 2, plan.units_per_head,
-                                                D == 128 ? 3 * ds->sms / 2 : 0)
-                           : BH;
-  const bool run_time_units = causal && (D == 256 || (D == 128 && group < BH));
+  int group = BH;
+  bool run_time_units = false;
+  if (causal) causal_order(BH, S, D, 2, plan.units_per_head, ds->sms, &group, &run_time_units);
   a.params.sched = run_time_units ? sched_pair(ds, a.stream) : nullptr;
-  a.params.group_heads = run_time_units ? group : BH;
+  a.params.group_heads = group;
 
   const cudaError_t e = D == 64    ? launch_fwd_d64(causal != 0, bf16, a)
                         : D == 128 ? launch_fwd_d128(causal != 0, bf16, a)
@@ -752,9 +780,11 @@ FATTN_API int fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   // as for 16-bit inputs at D = 128: units at run time only when the K and
   // V of all heads exceed one group
-  const int group = causal ? causal_group_heads(BH, S, D, units_per_head, 3 * ds->sms / 2) : BH;
-  a.params.sched = causal && group < BH ? sched_pair(ds, a.stream) : nullptr;
-  a.params.group_heads = a.params.sched != nullptr ? group : BH;
+  int group = BH;
+  bool run_time_units = false;
+  if (causal) causal_order(BH, S, D, 1, units_per_head, ds->sms, &group, &run_time_units);
+  a.params.sched = run_time_units ? sched_pair(ds, a.stream) : nullptr;
+  a.params.group_heads = group;
   if (launch_fwd_fp8_d128(causal != 0, out_dtype == FATTN_BF16, a) != cudaSuccess) {
     cudaGetLastError();
     return FATTN_ERR_LAUNCH;

@@ -176,6 +176,22 @@ FATTN_API int fattn_plan(int B, int H, int S, int D, int causal, int *grid,
                          int *q_tiles_per_unit, int *kv_stages);
 
 /*
+ * The order in which a causal launch of these sizes takes its work units on
+ * a device with ``sms`` SMs, without a device (the persistent grid of the
+ * "Lecture 6" FA2 change 1, parallelism over the sequence, longest units
+ * first).  elem_bytes is 2 for fattn_fwd (fp16/bf16) and 1 for fattn_fwd_fp8
+ * (D = 128).  Fills (each pointer may be NULL): *group_heads, the heads of
+ * one group of the order (B*H when every head is in one group; the groups
+ * differ by at most one head), and *run_time, 1 when the units are handed
+ * out at run time from a per-launch counter, 0 when each CTA takes the
+ * static longest-first snake.  Returns FATTN_OK, FATTN_ERR_INVALID_ARG (sms
+ * < 1, elem_bytes not 1 or 2), FATTN_ERR_UNSUPPORTED (E4M3 with D != 128)
+ * or the status fattn_plan returns for the same sizes.
+ */
+FATTN_API int fattn_causal_order(int B, int H, int S, int D, int elem_bytes,
+                                 int sms, int *group_heads, int *run_time);
+
+/*
  * Attention of a few new queries against a key/value cache ("FlashAttention
  * V2", section 6: inference with a KV cache, which FlashAttention serves with
  * its decoding variant; the per-row recurrence of section 3).
